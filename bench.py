@@ -1,0 +1,377 @@
+"""Benchmark of one Ulysses attention block training pass on GB300.
+
+One step = the whole hot path over one batch of synthetic input, all through the C ABI
+on one stream:
+  QKV projection -> seq->head (+RoPE) -> causal GQA attention forward (+lse) ->
+  head->seq of O -> seq->head of dO -> attention backward (dQ, dK, dV) ->
+  head->seq of dQ, dK, dV.
+Workload (default): the Llama-3.1-8B-shaped attention block at S=131072, P=8 virtual
+ranks, hidden 4096, 32 query / 8 KV heads, head_dim 128, RoPE theta 500000, bf16.
+Metric: causal attention fwd+bwd TFLOPS (algorithmic FLOPs: fwd 2*S^2*D*H, bwd 2.5x fwd)
+over the whole step time; the permute GB/s (read + write bytes) is reported beside it.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--seq S]    (S other than 131072 is for quick checks only)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = dict(name="llama3.1-8b-attention-block-fwd-bwd", S=131072, P=8, hidden=4096, H=32,
+                G=8, D=128, theta=500000.0)
+METRIC = "causal attn fwd+bwd TFLOPS at S=128K (whole step incl. projection and all-to-all permutes)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def attn_flops(S, H, D):
+    fwd = 2.0 * S * S * D * H          # causal: half of the dense 4 S^2 D H
+    return fwd, 2.5 * fwd
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------- CPU oracle leg
+def oracle_sample(S, H, D, n_rows, seed_stream=0):
+    """Times the oracle on a bounded sample of the workload: n_rows seed-sampled query rows
+    of one head (causal forward over the full prefix, then dq of those rows).  Returns
+    (algorithmic FLOPs of the sample, seconds, description)."""
+    import numpy as np
+
+    import oracle as O
+    import synthetic
+    rows = np.sort(synthetic.sample_rows(S, 8, n_rows, stream=seed_stream))[-n_rows:]
+    jmax = int(rows.max()) + 1
+    k = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_K, (jmax, 1, D), std=1.28))
+    v = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_V, (jmax, 1, D), std=1.28))
+    q = np.zeros((jmax, 1, D))
+    q[rows] = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_Q, (rows.size, 1, D), std=1.28))
+    do = np.zeros((jmax, 1, D))
+    do[rows] = synthetic.bf16_to_f64(synthetic.normal_bf16(1, 0, (rows.size, 1, D)))
+    t0 = time.perf_counter()
+    O.causal_attention_bwd_rows(q, k, v, do, rows, jmax)   # forward of the rows + their dq
+    dt = time.perf_counter() - t0
+    flops = 3.5 * float(np.sum(4.0 * (rows + 1) * D))      # fwd + 2.5x bwd, causal prefix
+    desc = ("%d seed-sampled query rows of one head at S=%d (fwd over the causal prefix + "
+            "dq of those rows), D=%d" % (rows.size, S, D))
+    return flops, dt, desc
+
+
+def run_reference(args):
+    """The oracle arm: each step is one bounded sample of the workload on the host cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOAD
+    S = args.seq or w["S"]
+    rows = 128
+    for _ in range(args.warmup):
+        oracle_sample(S, w["H"], w["D"], rows)
+    flops = secs = 0.0
+    desc = ""
+    for i in range(args.steps):
+        f, s, desc = oracle_sample(S, w["H"], w["D"], rows, seed_stream=i + 1)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    cores = host_cores()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w["name"], "seq_len": S, "P": w["P"], "hidden": w["hidden"],
+                       "n_q_heads": w["H"], "n_kv_heads": w["G"], "head_dim": w["D"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- GPU leg
+class ClockSampler:
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        try:
+            for line in open(self.path):
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx = float(f[2])
+                except ValueError:
+                    continue
+                for name, val in zip(("hw_slowdown", "hw_thermal_slowdown",
+                                      "sw_thermal_slowdown", "sw_power_cap"), f[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        except Exception:
+            pass
+        finally:
+            if self.path and os.path.exists(self.path):
+                os.remove(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import long_context_sequence_gb300 as U
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WORKLOAD
+    S, P, hidden, H, G, D, theta = (args.seq or w["S"]), w["P"], w["hidden"], w["H"], w["G"], w["D"], w["theta"]
+    plan = U.ulysses_plan(U.make_config(S, P, hidden, H, G, D, rope_theta=theta))
+    sh = plan.shapes()
+    bf = torch.bfloat16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    x = torch.randn(sh["x"], generator=gen, device=dev).to(bf)
+    wq = (torch.randn(sh["w"], generator=gen, device=dev) * 0.02).to(bf)
+    do_seq = torch.randn(sh["o_seq"], generator=gen, device=dev).to(bf)
+    qkv = torch.empty(sh["qkv"], dtype=bf, device=dev)
+    q, k, v = (torch.empty(sh[n], dtype=bf, device=dev) for n in ("q", "k", "v"))
+    o = torch.empty(sh["o"], dtype=bf, device=dev)
+    lse = torch.empty(sh["lse"], dtype=torch.float32, device=dev)
+    o_seq = torch.empty(sh["o_seq"], dtype=bf, device=dev)
+    do = torch.empty(sh["o"], dtype=bf, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dq_seq = torch.empty(sh["o_seq"], dtype=bf, device=dev)
+    dk_seq = torch.empty(sh["kv_seq"], dtype=bf, device=dev)
+    dv_seq = torch.empty(sh["kv_seq"], dtype=bf, device=dev)
+    ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sid = stream.cuda_stream
+    names = ["qkv_proj", "seq_to_head", "attn_fwd", "head_to_seq_o", "seq_to_head_do",
+             "attn_bwd", "head_to_seq_grads"]
+    launches_per_step = 1 + 1 + 1 + 1 + 1 + 3 + 3
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        U.ulysses_qkv_proj(plan, x, wq, qkv, sid)
+        mark(1)
+        U.ulysses_seq_to_head(plan, qkv, q, k, v, apply_rope=True, stream=sid)
+        mark(2)
+        U.ulysses_attn_fwd(plan, q, k, v, o, lse, sid)
+        mark(3)
+        U.ulysses_head_to_seq(plan, o, H, o_seq, sid)
+        mark(4)
+        U.ulysses_seq_to_head_heads(plan, do_seq, H, do, sid)
+        mark(5)
+        U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid)
+        mark(6)
+        U.ulysses_head_to_seq(plan, dq, H, dq_seq, sid)
+        U.ulysses_head_to_seq(plan, dk, G, dk_seq, sid)
+        U.ulysses_head_to_seq(plan, dv, G, dv_seq, sid)
+        mark(7)
+
+    for _ in range(args.warmup):
+        step()
+    st = U.ulysses_sync_status(plan, sid)
+    if st != U.ULY_OK:
+        raise RuntimeError("device status %d during warm-up: %s" % (st, U.ulysses_last_error()))
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = U.ulysses_sync_status(plan, sid)
+    if st != U.ULY_OK:
+        raise RuntimeError("device status %d: %s" % (st, U.ulysses_last_error()))
+    total_ms = t_start.elapsed_time(t_end)
+    per = {n: [] for n in names}
+    for e in evs:
+        for i, n in enumerate(names):
+            per[n].append(e[i].elapsed_time(e[i + 1]))
+    avg = {n: sum(vs) / len(vs) for n, vs in per.items()}
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    fwd_f, bwd_f = attn_flops(S, H, D)
+    value = world * (fwd_f + bwd_f) / (ms_step * 1e-3) / 1e12
+
+    # permute traffic per step (read + write bytes)
+    C = (H + 2 * G) * D
+    perm_bytes = {"seq_to_head": S * C * 2 * 2, "head_to_seq_o": S * H * D * 2 * 2,
+                  "seq_to_head_do": S * H * D * 2 * 2,
+                  "head_to_seq_grads": S * (H + 2 * G) * D * 2 * 2}
+    perm_ms = sum(avg[n] for n in perm_bytes)
+    perm_gbs = sum(perm_bytes.values()) / (perm_ms * 1e-3) / 1e9
+    peaks, peak_kind = load_peaks()
+    bwd_tflops = bwd_f / (avg["attn_bwd"] * 1e-3) / 1e12
+    fwd_tflops = fwd_f / (avg["attn_fwd"] * 1e-3) / 1e12
+    qkv_tflops = 2.0 * S * hidden * C / (avg["qkv_proj"] * 1e-3) / 1e12
+    s2h_gbs = perm_bytes["seq_to_head"] / (avg["seq_to_head"] * 1e-3) / 1e9
+
+    # end to end through the same calls, with the step's inputs coming from pinned host
+    # memory and its outputs read back, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.empty(sh["x"], dtype=bf, pin_memory=True)
+        hdo = torch.empty(sh["o_seq"], dtype=bf, pin_memory=True)
+        hx.copy_(x)
+        hdo.copy_(do_seq)
+        outs = [o_seq, dq_seq, dk_seq, dv_seq]
+        houts = [torch.empty(t.shape, dtype=bf, pin_memory=True) for t in outs]
+        h2d = hx.numel() * 2 + hdo.numel() * 2
+        d2h = sum(t.numel() * 2 for t in outs)
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            do_seq.copy_(hdo, non_blocking=True)
+            step()
+            for h_, d_ in zip(houts, outs):
+                h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": world * (fwd_f + bwd_f) / (ems * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        f, s, desc = oracle_sample(S, H, D, 512)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOPS", "cores": host_cores(), "kind": "oracle",
+               "sample": desc, "seconds": s}
+
+    if rank == 0:
+        peak = peaks["bf16_tflops_sustained"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (device torch.randn, seeded; X~N(0,1), W~N(0,0.02^2), dO~N(0,1))",
+            "config": {"workload": w["name"], "seq_len": S, "P": P, "hidden": hidden,
+                       "n_q_heads": H, "n_kv_heads": G, "head_dim": D, "rope_theta": theta,
+                       "global_batch": world, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (no flush)"},
+            "roofline": {"kernel": "ulysses_attn_bwd", "bound": "tensor",
+                         "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                         "frac": bwd_tflops / peak, "traffic": None,
+                         "peak_source": "%s bf16_tflops_sustained" % peak_kind},
+            "kernels_ms": avg,
+            "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
+            "attn_fwd_frac": fwd_tflops / peak, "qkv_proj_tflops": qkv_tflops,
+            "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / peaks["hbm_gbs"],
+            "seq_to_head_gbs": s2h_gbs, "peaks": peaks, "peaks_source": peak_kind,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line))
+    plan.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seq", type=int, default=0, help="override S (quick checks only)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours" and not args.seq:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/* Ulysses sequence-parallel attention block on one GPU: the C ABI.
+ *
+ * The method (web pages on Ulysses Sequence Parallelism; cited by title and paragraph):
+ *   "Snowflake's Ulysses trick trains transformers on million-token contexts across
+ *   GPUs", para 2: the sequence is sharded across P ranks; each rank computes its local
+ *   QKV projection; an all-to-all leaves every rank the full sequence for a subset of
+ *   the attention heads; since heads are independent each rank runs FlashAttention on
+ *   its heads; a second all-to-all restores the sequence sharding.  Para 3: two
+ *   all-to-alls per layer, total volume O(hidden x seq_len / P).
+ *   "Ulysses Sequence Parallelism: Training with Million-Token Contexts" (the Hugging
+ *   Face post): para 3 (attention is quadratic; FlashAttention tiles it and never
+ *   materialises the score matrix), para 5 (the second all-to-all reverses the first),
+ *   para 7 (heads are partitioned across GPUs), para 8 (the input is split along the
+ *   sequence dimension).
+ *
+ * Here the P ranks are virtual: P slices of one GPU's memory.  The all-to-alls are
+ * on-device permutation kernels and there is no inter-GPU collective.
+ *
+ * Notation: S tokens, P ranks, H query heads, G KV heads, D head_dim, C = (H + 2G) * D.
+ * Shards are contiguous (rank r owns tokens [r*S/P, (r+1)*S/P)); rank r's head group is
+ * query heads [r*H/P, (r+1)*H/P) and KV heads [r*G/P, (r+1)*G/P); query head h reads KV
+ * head h / (H/G).  Attention is causal (key j visible to query i iff j <= i).
+ *
+ * Tensor layouts (row-major, innermost last; "bf16" = 16-bit brain float storage):
+ *   x        [S][hidden]                 bf16   token rows; rank r's shard is rows r*S/P..
+ *   w        [C][hidden]                 bf16   projection weight, nn.Linear layout,
+ *                                               rows = q heads, then k heads, then v heads
+ *   qkv_seq  [P][S/P][H + 2G][D]         bf16   (or fp32 when in_fp32): = [S][C]
+ *   q        [P][S][H/P][D]              bf16   rank r2's query heads for all tokens
+ *   k, v     [P][S][G/P][D]              bf16
+ *   o        [P][S][H/P][D]              bf16
+ *   lse      [P][H/P][S]                 fp32   natural-log logsumexp of each score row
+ *   o_seq    [P][S/P][H][D]              bf16   = [S][H][D]
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers to caller-owned memory, 16-byte aligned.  The library
+ *     never frees or keeps them past the call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ *     stream) and return a uly_status at once.  They never throw or exit.
+ *   - On error nothing is launched and ulysses_last_error() describes the problem (a
+ *     thread-local string valid until the next call on the same thread).
+ *   - Device-side failures (a wait that ran out, an unexpected layout) are recorded in a
+ *     status word held by the plan; ulysses_sync_status() reads and clears it.
+ *   - S = 0 is valid: every call is a no-op that returns ULY_OK.
+ */
+#ifndef ULYSSES_H_
+#define ULYSSES_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum uly_status {
+  ULY_OK = 0,
+  ULY_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer */
+  ULY_ERR_UNSUPPORTED = 2,  /* valid in principle, not built here (e.g. D not 64/128) */
+  ULY_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
+  ULY_ERR_OOM = 4,          /* the plan could not allocate its own small buffers */
+  ULY_ERR_TIMEOUT = 5       /* a device-side wait ran past its limit (from sync_status) */
+} uly_status;
+
+/* Plan flags. */
+#define ULY_FLAG_INJECT_STALL 0x1u /* test only: attn_fwd's MMA issuer withholds its first
+                                      score-ready signal, so the bounded waits run out */
+
+typedef struct uly_config {
+  int64_t seq_len;        /* S, tokens over all ranks; S % P == 0 */
+  int32_t batch;          /* must be 1 */
+  int32_t P;              /* virtual ranks (>= 1) */
+  int32_t hidden;         /* width of x and of the rows of w; multiple of 8 */
+  int32_t n_q_heads;      /* H; H % P == 0 and H % G == 0 */
+  int32_t n_kv_heads;     /* G; G % P == 0 */
+  int32_t head_dim;       /* D: 64 or 128 */
+  int32_t causal;         /* must be 1 */
+  int32_t wait_timeout_ms;/* limit of every device-side wait; 0 means 2000 */
+  double softmax_scale;   /* 0 means 1/sqrt(D) */
+  double rope_theta;      /* > 0 enables rotate-half RoPE in seq_to_head; 0 disables */
+  uint32_t flags;         /* ULY_FLAG_* */
+  uint32_t reserved;      /* must be 0 */
+} uly_config;
+
+typedef struct uly_plan_s *uly_plan;
+
+/* Validate cfg and build a plan: copies cfg, builds the RoPE angle tables (fp64 on the
+ * host, stored fp32 on the device) and a device status word.  No kernel is launched.
+ * Returns ULY_ERR_INVALID_ARG / ULY_ERR_UNSUPPORTED for bad configs, ULY_ERR_OOM or
+ * ULY_ERR_CUDA if its buffers cannot be made.  The current CUDA device is the plan's. */
+uly_status ulysses_plan(const uly_config *cfg, uly_plan *out);
+
+/* Frees the plan's buffers.  NULL is allowed.  Synchronises the device first. */
+uly_status ulysses_plan_destroy(uly_plan plan);
+
+/* Bytes of scratch that ulysses_attn_bwd needs: an fp32 dQ accumulator [P][S][H/P][D]
+ * followed by the fp32 row terms Delta [P][H/P][S], each part 256-byte aligned. */
+size_t ulysses_workspace_bytes(uly_plan plan);
+
+/* Local QKV projection of every shard ("each rank computes its local QKV projection",
+ * Ulysses-trick page para 2): qkv[s][c] = sum_k x[s][k] * w[c][k], fp32 accumulation,
+ * bf16 round-to-nearest-even output.  x [S][hidden], w [C][hidden], qkv [S][C] = the
+ * qkv_seq layout.  All ranks share w, so this is one GEMM over all S rows. */
+uly_status ulysses_qkv_proj(uly_plan plan, const void *x, const void *w, void *qkv,
+                            void *stream);
+
+/* seq->head all-to-all (Ulysses-trick page para 2): for every token s of rank r and
+ * column head c, writes q[c/(H/P)][s][c%(H/P)] (query heads), k[..][s][..] and v.
+ * in_fp32 != 0: qkv_seq is fp32 and is rounded to bf16 (RNE) on the way.
+ * apply_rope != 0 (needs rope_theta > 0): q and k rows are rotated (rotate-half form) by
+ * angle s * theta^(-2i/D) for the pair (i, i + D/2), s the global token index, in fp32,
+ * then rounded to bf16.  Without RoPE the permutation moves bits unchanged. */
+uly_status ulysses_seq_to_head(uly_plan plan, const void *qkv_seq, int in_fp32,
+                               int apply_rope, void *q, void *k, void *v, void *stream);
+
+/* seq->head all-to-all of one tensor of n_heads heads (n_heads = H or G; e.g. the
+ * upstream gradient dO): x_seq [P][S/P][n_heads][D] -> x_head [P][S][n_heads/P][D]. */
+uly_status ulysses_seq_to_head_heads(uly_plan plan, const void *x_seq, int n_heads,
+                                     void *x_head, void *stream);
+
+/* Causal GQA attention of every rank's head group over the full sequence ("each GPU can
+ * compute its share using standard FlashAttention locally", Ulysses-trick page para 2;
+ * tiled so no S x S matrix is ever stored, Hugging Face post para 3).  For query head
+ * h' of rank r (KV head h' / (H/G)):  o = softmax(scale * q k^T, causal) v in bf16 with
+ * fp32 softmax and accumulation; lse = natural-log logsumexp of the scaled scores. */
+uly_status ulysses_attn_fwd(uly_plan plan, const void *q, const void *k, const void *v,
+                            void *o, float *lse, void *stream);
+
+/* Backward of ulysses_attn_fwd for the training step (Hugging Face post para 1: the
+ * method is for training).  Inputs q, k, v, o, lse as above and the upstream gradient
+ * d_o in head layout [P][S][H/P][D].  Outputs dq [P][S][H/P][D], dk, dv [P][S][G/P][D]
+ * in bf16; dk and dv sum the contributions of all query heads of a KV head.
+ * workspace: ulysses_workspace_bytes(plan) bytes of device memory (fp32 accumulators);
+ * its contents on entry do not matter. */
+uly_status ulysses_attn_bwd(uly_plan plan, const void *q, const void *k, const void *v,
+                            const void *o, const float *lse, const void *d_o, void *dq,
+                            void *dk, void *dv, void *workspace, void *stream);
+
+/* head->seq all-to-all, the inverse of seq->head ("another all-to-all operation reverses
+ * the redistribution", Hugging Face post para 5): x_head [P][S][n_heads/P][D] ->
+ * x_seq [P][S/P][n_heads][D].  n_heads = H for o and dq, G for dk and dv. */
+uly_status ulysses_head_to_seq(uly_plan plan, const void *x_head, int n_heads, void *x_seq,
+                               void *stream);
+
+/* Synchronises `stream`, reads the plan's device status word, clears it and returns it
+ * (ULY_OK, or e.g. ULY_ERR_TIMEOUT).  ULY_ERR_CUDA if the synchronisation itself fails. */
+uly_status ulysses_sync_status(uly_plan plan, void *stream);
+
+/* Bytes read plus written by this plan's permute kernels since it was made: what the
+ * all-to-all kernels move through HBM. */
+uint64_t ulysses_bytes_moved(uly_plan plan);
+
+/* Per-rank all-to-all volume of one block (Ulysses-trick page para 3): the bytes one
+ * rank sends to other ranks in the seq->head exchange ((S/P) * (H + 2G) * D * 2 *
+ * (P-1)/P) and in the head->seq exchange ((S/P) * H * D * 2 * (P-1)/P). */
+uly_status ulysses_a2a_volume(const uly_config *cfg, uint64_t *seq_to_head_bytes,
+                              uint64_t *head_to_seq_bytes);
+
+/* Description of the last error on this thread ("" if none). */
+const char *ulysses_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H_ */

@@ -1,0 +1,360 @@
+// Causal GQA attention forward of every virtual rank's head group, with logsumexp.
+//
+// "Snowflake's Ulysses trick ..." para 2: after the seq->head all-to-all each rank holds
+// the full sequence for its heads, and "since attention heads are independent" runs
+// FlashAttention on them locally.  "Ulysses Sequence Parallelism: Training with
+// Million-Token Contexts" para 3: tiling never materialises the S x S score matrix.
+//
+// Design (sm_103a, tcgen05):
+//   * one CTA = one (rank, query head, 256-row block) as two 128-row query tiles Q0, Q1
+//     that share every K/V tile; blocks are issued heaviest (longest causal prefix) first
+//     and neighbouring blocks are the query heads of one KV head, so K/V stay in L2;
+//   * warp 8 (TMA): Q0/Q1 once, then K_j and V_j into a 2-deep ring (128-byte swizzle);
+//   * warp 9 (MMA, one thread): S_t = Q_t K_j^T into TMEM (fp32, 128 columns each), then
+//     O_t += P_t V_j with P_t read from TMEM (bf16, written over S_t);
+//   * warps 0-3 / 4-7: the online softmax of Q0 / Q1, one thread per row (= TMEM lane),
+//     in the log2 domain, with lazy rescaling of O (only when the running max grows by
+//     more than 2^8); they also write O / l and lse at the end;
+//   * causal tile skipping: Q0 sees KV tiles 0..m0/128, Q1 one more.
+// TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D) of 512 columns.
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+#include "uly_internal.h"
+
+namespace uly {
+namespace {
+
+constexpr int BM = 128, BN = 128;
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kBox = 128 * 64 * 2;   // one [128 rows][64 elements] bf16 box
+
+template <int D>
+struct Layout {
+  static constexpr int kTile = (D / 64) * kBox;
+  static constexpr int kQ = 0;
+  static constexpr int kK = 2 * kTile;
+  static constexpr int kV = 4 * kTile;
+  static constexpr int kBar = 6 * kTile;
+  static constexpr int kBytes = kBar + 256 + 1024;
+};
+
+struct FwdArgs {
+  __nv_bfloat16* o;
+  float* lse;
+  int S, hl, gl, group, n_mb;
+  float scale_log2;
+  int* status;
+  uint64_t limit_ns;
+  uint32_t flags;
+};
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;    // [2]
+  uint64_t* k_empty = bars + 3;   // [2]
+  uint64_t* v_full = bars + 5;    // [2]
+  uint64_t* v_empty = bars + 7;   // [2]
+  uint64_t* s_full = bars + 9;    // [2] one per query tile
+  uint64_t* p_full = bars + 11;   // [2]
+  uint64_t* o_done = bars + 13;   // [2]
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // Block -> (rank, local query head, 256-row block), heaviest blocks first.
+  const int per_rank = a.hl * a.n_mb;
+  const int r = blockIdx.x / per_rank;
+  const int rem = blockIdx.x - r * per_rank;
+  const int mb = a.n_mb - 1 - rem / a.hl;
+  const int hh = rem % a.hl;
+  const int gg = hh / a.group;
+  const int m0 = mb * 2 * BM;
+  const int n_kv = (a.S + BN - 1) / BN;
+  const int n0 = min(m0 / BN + 1, n_kv);
+  const int n1 = min(m0 / BN + 2, n_kv);
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&o_done[i], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const WaitCtl wc{a.status, abort_flag, a.limit_ns};
+
+  if (warp == kTmaWarp) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      mbar_arrive_expect_tx(q_full, 2 * L::kTile);
+      for (int t = 0; t < 2; ++t)
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_4d(smem + L::kQ + t * L::kTile + b * kBox, &tm_q, q_full, 64 * b, hh,
+                      m0 + t * BM, r);
+      int k_issued = 0, v_issued = 0;
+      for (int j = 0; j < n1; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (j >= 2 && !mbar_wait(&k_empty[st], ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::kTile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_4d(smem + L::kK + st * L::kTile + b * kBox, &tm_k, &k_full[st], 64 * b, gg,
+                      j * BN, r);
+        ++k_issued;
+        if (j >= 2 && !mbar_wait(&v_empty[st], ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&v_full[st], L::kTile);
+        for (int b = 0; b < D / 64; ++b)
+          tma_load_4d(smem + L::kV + st * L::kTile + b * kBox, &tm_v, &v_full[st], 64 * b, gg,
+                      j * BN, r);
+        ++v_issued;
+      }
+      // Every issued copy lands before exit (immediate on the normal path).
+      mbar_drain(q_full, 0, a.limit_ns);
+      for (int j = k_issued > 2 ? k_issued - 2 : 0; j < k_issued; ++j)
+        mbar_drain(&k_full[j & 1], (j >> 1) & 1, a.limit_ns);
+      for (int j = v_issued > 2 ? v_issued - 2 : 0; j < v_issued; ++j)
+        mbar_drain(&v_full[j & 1], (j >> 1) & 1, a.limit_ns);
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
+      const bool stall = (a.flags & ULY_FLAG_INJECT_STALL) && blockIdx.x == 0;
+      bool alive = mbar_wait(q_full, 0, wc);
+      auto issue_s = [&](int t, int j) {
+        const uint32_t qa = smem_u32(smem + L::kQ + t * L::kTile);
+        const uint32_t kb = smem_u32(smem + L::kK + (j & 1) * L::kTile);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
+          mma_ss(tbase + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                 idesc_qk, kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int j) -> bool {
+        if (!mbar_wait(&p_full[t], j & 1, wc)) return false;
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + L::kV + (j & 1) * L::kTile);
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tbase + 2 * BN + t * D, tbase + t * BN + kk * 8,
+                 sdesc_sw128(vb + kk * 16 * 128, kBox, 1024), idesc_pv,
+                 (j > 0 || kk > 0) ? 1u : 0u);
+        return true;
+      };
+      for (int j = 0; alive && j < n1; ++j) {
+        if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, wc)) { alive = false; break; }
+        tc_fence_after();
+        for (int t = 0; t < 2 && alive; ++t) {
+          const int nt = t ? n1 : n0;
+          if (j < nt) {
+            if (j >= 1 && !issue_pv(t, j - 1)) { alive = false; break; }
+            issue_s(t, j);
+            if (!(stall && j == 0 && t == 0)) mma_commit(&s_full[t]);
+          } else if (j == nt) {
+            if (!issue_pv(t, j - 1)) { alive = false; break; }
+            mma_commit(&o_done[t]);
+          }
+        }
+        if (!alive) break;
+        mma_commit(&k_empty[j & 1]);
+        if (j >= 1) mma_commit(&v_empty[(j - 1) & 1]);
+      }
+      for (int t = 0; t < 2 && alive; ++t) {
+        const int nt = t ? n1 : n0;
+        if (nt == n1) {
+          if (!issue_pv(t, n1 - 1)) { alive = false; break; }
+          mma_commit(&o_done[t]);
+        }
+      }
+      // All issued MMAs complete before TMEM can be freed.
+      mma_commit(drain);
+      mbar_drain(drain, 0, a.limit_ns);
+    }
+  } else {
+    // Softmax warpgroups: t = query tile, one thread per row / TMEM lane.
+    const int t = warp / 4;
+    const int lane_base = (warp % 4) * 32;
+    const int row = lane_base + lane;
+    const int row_g = m0 + t * BM + row;
+    const int nt = t ? n1 : n0;
+    const uint32_t ts = tbase + ((uint32_t)lane_base << 16) + t * BN;
+    const uint32_t to = tbase + ((uint32_t)lane_base << 16) + 2 * BN + t * D;
+    const float sl2 = a.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, wc));
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t s[4][32];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(ts + 32 * c, s[c]);
+      const int kbase = j * BN;
+      if (kbase + BN - 1 > m0 + t * BM || kbase + BN > a.S) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int kp = kbase + 32 * c + i;
+            if (kp > row_g || kp >= a.S) s[c][i] = __float_as_uint(-INFINITY);
+          }
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
+      const float m_new = fmaxf(m_used, mx * sl2);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (j == 0) {
+        m_used = m_new;
+      } else if (m_new > m_used + 8.f) {
+        alpha = ex2_approx(m_used - m_new);
+        m_used = m_new;
+        rescale = true;
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i]), sl2, -m_used));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, -m_used));
+          sum += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(ts + 16 * c, pk);
+      }
+      l = l * alpha + sum;
+      if (rescale) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(to + 32 * c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(to + 32 * c, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[t]);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0, wc));
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = 1.f / l;
+      __nv_bfloat16* orow = a.o + (((size_t)r * a.S + row_g) * a.hl + hh) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(to + 32 * c, o);
+        if (row_g < a.S) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(o[8 * j + 0]) * inv_l, __uint_as_float(o[8 * j + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(o[8 * j + 2]) * inv_l, __uint_as_float(o[8 * j + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv_l, __uint_as_float(o[8 * j + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv_l, __uint_as_float(o[8 * j + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + 32 * c + 8 * j) = v;
+          }
+        }
+      }
+      if (row_g < a.S)
+        a.lse[((size_t)r * a.hl + hh) * a.S + row_g] = (m_used + lg2_approx(l)) * 0.6931471805599453f;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_fwd_d(const Plan& p, const void* q, const void* k, const void* v, void* o,
+                         float* lse, cudaStream_t st) {
+  const int hl = p.H / p.P, gl = p.G / p.P;
+  const char* err = nullptr;
+  CUtensorMap tq, tk, tv;
+  const uint64_t dq[4] = {(uint64_t)D, (uint64_t)hl, (uint64_t)p.S, (uint64_t)p.P};
+  const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)hl * D * 2, (uint64_t)p.S * hl * D * 2};
+  const uint64_t dk[4] = {(uint64_t)D, (uint64_t)gl, (uint64_t)p.S, (uint64_t)p.P};
+  const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)gl * D * 2, (uint64_t)p.S * gl * D * 2};
+  if (!make_tmap_4d_bf16(&tq, q, dq, sq, 64, BM, &err) ||
+      !make_tmap_4d_bf16(&tk, k, dk, sk, 64, BN, &err) ||
+      !make_tmap_4d_bf16(&tv, v, dk, sk, 64, BN, &err))
+    return cudaErrorInvalidValue;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o);
+  a.lse = lse;
+  a.S = (int)p.S;
+  a.hl = hl;
+  a.gl = gl;
+  a.group = p.H / p.G;
+  a.n_mb = (int)((p.S + 2 * BM - 1) / (2 * BM));
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.status = p.status;
+  a.limit_ns = p.limit_ns;
+  a.flags = p.cfg.flags;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Layout<D>::kBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (int64_t)p.P * hl * a.n_mb;
+  attn_fwd_kernel<D><<<(unsigned)blocks, kThreads, Layout<D>::kBytes, st>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v, void* o,
+                            float* lse, cudaStream_t st) {
+  if (p.D == 64) return launch_fwd_d<64>(p, q, k, v, o, lse, st);
+  return launch_fwd_d<128>(p, q, k, v, o, lse, st);
+}
+
+}  // namespace uly

@@ -1,0 +1,61 @@
+// Internal declarations shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <atomic>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ulysses.h"
+
+namespace uly {
+
+// RoPE angles are kept as a two-level table so that positions up to 2^20 and beyond
+// need little memory: for s = sh * kRopeL + sl, (cos, sin)(s * w_i) is rebuilt from
+// hi[sh][i] = (cos, sin)(sh * kRopeL * w_i) and lo[sl][i] = (cos, sin)(sl * w_i) by the
+// angle-addition identities (fp64 on the host, fp32 in the table).
+constexpr int kRopeL = 1024;
+
+struct Plan {
+  uly_config cfg;
+  int device = 0;
+  int64_t S = 0;
+  int P = 1, hidden = 0, H = 0, G = 0, D = 0;
+  float scale = 0.f;
+  float2* rope_hi = nullptr;   // [ceil(S / kRopeL)][D/2]
+  float2* rope_lo = nullptr;   // [kRopeL][D/2]
+  int* status = nullptr;       // device status word
+  uint64_t limit_ns = 0;
+  std::atomic<uint64_t> bytes_moved{0};
+};
+
+// Launchers: each validates nothing (api.cu did) and returns the launch error.
+cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool rope, void* q,
+                               void* k, void* v, cudaStream_t st);
+cudaError_t launch_permute_heads(const Plan& p, const void* in, int n_heads, void* out,
+                                 bool to_head, cudaStream_t st);
+cudaError_t launch_qkv_gemm(const Plan& p, const void* x, const void* w, void* out,
+                            cudaStream_t st);
+cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v,
+                            void* o, float* lse, cudaStream_t st);
+cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const void* v,
+                            const void* o, const float* lse, const void* d_o, void* dq,
+                            void* dk, void* dv, void* workspace, cudaStream_t st);
+
+// Workspace layout of the backward pass.
+size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off);
+
+// Tensor maps (TMA descriptors), built on the host through the driver entry point.
+// Returns false and sets *err on failure.
+bool make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                       const char** err);
+// 4-D bf16 map over [d3][d2][d1][d0] (d0 innermost) with byte strides s1, s2, s3 and a box
+// of {box0, 1, box2, 1}; 128-byte swizzle, out-of-range elements read as zero.
+bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4],
+                       const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
+                       const char** err);
+
+int num_sms(int device);
+
+}  // namespace uly

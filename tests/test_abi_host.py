@@ -1,0 +1,79 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports every symbol
+that include/ulysses.h declares, validates configs and reports the all-to-all volume."""
+import os
+import re
+
+import pytest
+
+import long_context_sequence_gb300 as U
+import oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build_library()
+    return U.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "ulysses.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ulysses_\w+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert len(names) >= 13
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(names) == sorted(U.EXPORTED)
+
+
+def test_config_validation_errors(lib):
+    good = dict(seq_len=1024, P=4, hidden=512, n_q_heads=8, n_kv_heads=8, head_dim=64)
+    cases = [
+        (dict(n_kv_heads=6), U.ULY_ERR_INVALID_ARG),        # H % G
+        (dict(n_q_heads=6, n_kv_heads=6), U.ULY_ERR_INVALID_ARG),   # H % P
+        (dict(n_q_heads=8, n_kv_heads=2), U.ULY_ERR_UNSUPPORTED),   # G % P: replication
+        (dict(head_dim=96), U.ULY_ERR_UNSUPPORTED),
+        (dict(hidden=100), U.ULY_ERR_INVALID_ARG),
+        (dict(seq_len=1022), U.ULY_ERR_INVALID_ARG),          # S % P
+        (dict(P=0), U.ULY_ERR_INVALID_ARG),
+        (dict(seq_len=-4), U.ULY_ERR_INVALID_ARG),
+    ]
+    for over, status in cases:
+        cfg = U.make_config(**{**good, **over})
+        with pytest.raises(U.UlyssesError) as ei:
+            U.ulysses_a2a_volume(cfg)
+        assert ei.value.status == status, (over, ei.value)
+    cfg = U.make_config(**good)
+    cfg.batch = 2
+    with pytest.raises(U.UlyssesError) as ei:
+        U.ulysses_a2a_volume(cfg)
+    assert ei.value.status == U.ULY_ERR_UNSUPPORTED
+    cfg = U.make_config(**good)
+    cfg.causal = 0
+    with pytest.raises(U.UlyssesError):
+        U.ulysses_a2a_volume(cfg)
+    cfg = U.make_config(**good, flags=0x80)
+    with pytest.raises(U.UlyssesError):
+        U.ulysses_a2a_volume(cfg)
+
+
+@pytest.mark.parametrize("S,P,H,G,D", [(1024, 4, 8, 8, 64), (32768, 8, 32, 8, 128),
+                                       (131072, 8, 32, 8, 128), (4096, 1, 8, 8, 128)])
+def test_a2a_volume_matches_oracle_closed_form(lib, S, P, H, G, D):
+    got = U.ulysses_a2a_volume(U.make_config(S, P, 4096, H, G, D))
+    assert got == O.a2a_volume_bytes(S, P, H, G, D)
+
+
+def test_null_plan_is_rejected(lib):
+    class Fake:
+        handle = None
+    with pytest.raises(U.UlyssesError) as ei:
+        U.ulysses_attn_fwd(Fake(), 0, 0, 0, 0, 0, stream=0)
+    assert ei.value.status == U.ULY_ERR_INVALID_ARG
+    assert "plan" in U.ulysses_last_error()
