@@ -266,7 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(ts + 16 * c, pk);
       }
       l = l * alpha + sum;
-      if (rescale) {
+      // tcgen05.ld/st are warp-collective: the whole warp rescales when any row needs it
+      // (rows that do not need it have alpha = 1).
+      if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];

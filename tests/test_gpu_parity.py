@@ -55,7 +55,7 @@ def test_permutes_bit_exact(S, P, H, G, D):
     U.ulysses_seq_to_head_heads(plan, back_q, H, q2)
     _ok(plan)
     assert np.array_equal(host_bits(q2), oq)
-    expect = S * (H + 2 * G) * D * 4 + 3 * S * H * D * 4 + S * G * D * 4
+    expect = S * (H + 2 * G) * D * 4 + 2 * S * H * D * 4 + S * G * D * 4
     assert U.ulysses_bytes_moved(plan) == expect
 
 
@@ -84,9 +84,12 @@ def test_seq_to_head_rope_within_one_ulp(S, P, H, G, D, theta):
     rot = np.concatenate([O.apply_rope(xf[:, :H + G], pos, theta), xf[:, H + G:]], axis=1)
     oq, ok, ov = O.seq_to_head(rot, P, H, G)
     for got, ref in ((q, oq), (k, ok)):
-        ref_bits = synthetic.f32_to_bf16(ref.astype(np.float32))
-        dist = bf16_ulp_distance(host_bits(got), ref_bits)
-        assert dist.max() <= 1, "RoPE error %d ulp" % dist.max()
+        # fp32 rotation then one bf16 rounding: within one bf16 ulp of the exact value
+        # (ulp taken at the exact value's magnitude) plus the fp32 rotation error
+        err = np.abs(host_f64(got) - ref)
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+        bound = ulp + 1e-5
+        assert np.all(err <= bound), "RoPE error %.3g ulp" % (err / ulp).max()
     assert np.array_equal(host_bits(v), O.seq_to_head(x, P, H, G)[2])   # v untouched
 
 
