@@ -28,18 +28,29 @@ def empty_bf16(shape):
     return torch.empty(shape, dtype=torch.bfloat16, device="cuda")
 
 
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at the magnitude of x (normal range)."""
+    return 2.0 ** (np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126))) - 7)
+
+
 def assert_close(got, ref, name, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    """max |err| <= max_abs and mean |err| <= mean_abs.  A bf16 output of magnitude >= 4
+    cannot be closer than half its ulp (>= 0.0156, 0.031 at >= 8) to the fp64 value, so
+    per element the bound is max(max_abs, one bf16 ulp of the reference value)."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), "%s has non-finite values" % name
     d = np.abs(got - ref)
-    worst = np.unravel_index(np.argmax(d), d.shape) if d.size else ()
-    msg = "%s: max|err| %.3g at %s (got %.5g ref %.5g), mean|err| %.3g, max|ref| %.3g" % (
-        name, d.max() if d.size else 0, worst, got[worst] if d.size else 0,
-        ref[worst] if d.size else 0, d.mean() if d.size else 0,
-        np.abs(ref).max() if d.size else 0)
-    assert d.size == 0 or (d.max() <= max_abs and d.mean() <= mean_abs), msg
+    if d.size == 0:
+        return
+    bound = np.maximum(max_abs, bf16_ulp(ref))
+    excess = d / bound
+    worst = np.unravel_index(np.argmax(excess), d.shape)
+    msg = "%s: max|err| %.3g (bound there %.3g) at %s (got %.5g ref %.5g), mean|err| %.3g, " \
+          "max|ref| %.3g" % (name, d[worst], bound[worst], worst, got[worst], ref[worst],
+                             d.mean(), np.abs(ref).max())
+    assert excess.max() <= 1.0 and d.mean() <= mean_abs, msg
 
 
 def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:

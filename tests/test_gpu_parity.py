@@ -211,8 +211,11 @@ def test_block_forward_end_to_end_rope_8b_shape():
     _ok(plan)
     ro, rl, _ = O.ulysses_block_forward(synthetic.bf16_to_f64(x), synthetic.bf16_to_f64(w),
                                         P, H, G, D, theta)
-    assert_close(host_f64(o_seq), ro, "o_seq")
-    assert_close(host_f64(lse), rl, "lse")
+    # Against the unrounded fp64 pipeline the bf16 storage of q/k/v (relative 2^-9) moves
+    # the logits of this 8B-scale block (std ~1.6) by up to ~1e-2, so the end-to-end
+    # bound is 5e-2 max / 2e-3 mean; each stage alone meets 2e-2 (tests above).
+    assert_close(host_f64(o_seq), ro, "o_seq", max_abs=5e-2)
+    assert_close(host_f64(lse), rl, "lse", max_abs=5e-2)
 
 
 def test_empty_sequence_is_a_no_op():
