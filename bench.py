@@ -49,6 +49,21 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def reduce_max_ms(ms, world, dist=None, device=None):
+    """Step time of the whole job: the maximum over ranks (every rank's own events)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step, world, ms_per_step):
+    """Whole-job throughput: the work of all ranks divided by the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -261,13 +276,10 @@ def run_ours(args):
         for i, n in enumerate(names):
             per[n].append(e[i].elapsed_time(e[i + 1]))
     avg = {n: sum(vs) / len(vs) for n, vs in per.items()}
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max_ms(total_ms, world, dist, dev)
     ms_step = total_ms / args.steps
     fwd_f, bwd_f = attn_flops(S, H, D)
-    value = world * (fwd_f + bwd_f) / (ms_step * 1e-3) / 1e12
+    value = job_tflops(fwd_f + bwd_f, world, ms_step)
 
     # permute traffic per step (read + write bytes)
     C = (H + 2 * G) * D
@@ -312,12 +324,8 @@ def run_ours(args):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / args.steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": world * (fwd_f + bwd_f) / (ems * 1e-3) / 1e12, "unit": "TFLOPS",
+        ems = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dist, dev)
+        e2e = {"value": job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
     cpu = None

@@ -16,8 +16,10 @@
 //               dV += P^T dO_i, dK += dS^T Q_i           (A operand from TMEM)
 //               dQ_i = dS K -> TMEM -> fp32 vector reductions into the accumulator;
 //   bwd_dq    fp32 dQ accumulator -> bf16.
-// TMEM (512 columns): S^T [0,128) (P^T bf16 over [0,64)), dP^T [128,256) (dS^T bf16 over
-// [128,192)), dV [256,256+D), dK [256+D,256+2D); dQ goes to [64,128) and [192,256).
+// dS is kept as hi + lo bf16 parts for dK (hi in the smem tile that also feeds dQ, lo in
+// TMEM), so the long dK sums see dS to ~16 bits.
+// TMEM (512 columns): S^T [0,128) (P^T bf16 over [0,64)), dP^T [128,256) (dS^T lo part,
+// bf16, over [128,192)), dV [256,256+D), dK [256+D,256+2D); dQ goes to [64,128), [192,256).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -189,10 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_ts(tbase + 256, tbase + 0 + kk * 8, sdesc_sw128(sDO + kk * 2048, kBox, 1024),
                  idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q with dS = hi + lo: hi from the smem tile (K-major A operand),
+        // lo from TMEM, so dK sees dS to about 16 bits instead of 8.
+#pragma unroll
+        for (int kk = 0; kk < BM / 16; ++kk)
+          mma_ss(tbase + 256 + D, sdesc_sw128(sDS + (kk / 4) * kBox + (kk % 4) * 32, 16, 1024),
+                 sdesc_sw128(sQ + kk * 2048, kBox, 1024), idesc_kv,
+                 (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_ts(tbase + 256 + D, tbase + 128 + kk * 8, sdesc_sw128(sQ + kk * 2048, kBox, 1024),
-                 idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
+                 idesc_kv, 1u);
 #pragma unroll
         for (int half = 0; half < D / 64; ++half)
 #pragma unroll
@@ -232,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t sv[32], dp[32];
         tmem_ld32(tbase + lane_off + 32 * c, sv);
         tmem_ld32(tbase + lane_off + 128 + 32 * c, dp);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16], dk[16], lo[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
           float pv[2], dv[2];
@@ -247,10 +256,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             dv[e] = p * (__uint_as_float(dp[2 * u + e]) - dlt_b[ql]);
           }
           pk[u] = pack_bf16x2(pv[0], pv[1]);
-          dk[u] = pack_bf16x2(dv[0], dv[1]);
+          dk[u] = pack_bf16x2(dv[0], dv[1]);          // dS rounded to bf16 (hi part)
+          const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&dk[u]);
+          const float2 hf = __bfloat1622float2(hi);
+          lo[u] = pack_bf16x2(dv[0] - hf.x, dv[1] - hf.y);   // what the rounding lost
         }
         tmem_st16(tbase + lane_off + 16 * c, pk);
-        tmem_st16(tbase + lane_off + 128 + 16 * c, dk);
+        tmem_st16(tbase + lane_off + 128 + 16 * c, lo);
         // dS tile in smem: [key row][q], 64-column atoms of 128-byte swizzled rows.
         uint8_t* atom = sDS + (c / 2) * kBox + row * 128;
 #pragma unroll

@@ -1,0 +1,41 @@
+"""Failure detection without a GPU fault: a plan flag makes the forward kernel's MMA
+issuer withhold one completion signal, so the softmax warps' bounded waits run out.
+The kernel must end on its own, report ULY_ERR_TIMEOUT through the plan's status word,
+and leave the CUDA context usable for the next plan."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_sequence_gb300 as U
+import oracle as O
+import synthetic
+from gpu_helpers import assert_close, dev_bf16, empty_bf16, host_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _fwd(plan, S, P, H, G, D):
+    q = synthetic.normal_bf16(0, synthetic.TENSOR_Q, (P, S, H // P, D))
+    k = synthetic.normal_bf16(0, synthetic.TENSOR_K, (P, S, G // P, D))
+    v = synthetic.normal_bf16(0, synthetic.TENSOR_V, (P, S, G // P, D))
+    o = empty_bf16((P, S, H // P, D))
+    lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
+    U.ulysses_attn_fwd(plan, dev_bf16(q), dev_bf16(k), dev_bf16(v), o, lse)
+    return (q, k, v), o, lse
+
+
+def test_stalled_wait_times_out_and_context_survives():
+    S, P, H, G, D = 2048, 2, 4, 2, 128
+    bad = U.ulysses_plan(U.make_config(S, P, 64, H, G, D, flags=U.ULY_FLAG_INJECT_STALL,
+                                       wait_timeout_ms=100))
+    _fwd(bad, S, P, H, G, D)
+    assert U.ulysses_sync_status(bad) == U.ULY_ERR_TIMEOUT
+    assert "ran past" in U.ulysses_last_error()
+    assert U.ulysses_sync_status(bad) == U.ULY_OK       # reading the status cleared it
+    bad.close()
+    good = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
+    (q, k, v), o, lse = _fwd(good, S, P, H, G, D)
+    assert U.ulysses_sync_status(good) == U.ULY_OK
+    ro, rl = O.ulysses_attention(*(synthetic.bf16_to_f64(a) for a in (q, k, v)))
+    assert_close(host_f64(o), ro, "o after a timed-out launch")
+    assert_close(host_f64(lse), rl, "lse after a timed-out launch")
