@@ -1,0 +1,175 @@
+"""Parity at the full workload sizes, in the launch configuration the benchmark times.
+
+The GPU runs every row; the fp64 oracle checks seed-sampled query rows (plus the shard
+edges) one by one, the key rows of the sequence tail exactly, and properties that hold at
+any size (the seq->head->seq round trip is the identity bit for bit).  Inputs come from
+the seeded host generator, except the 12.9 GB full-hidden activation of the million-token
+permute, which is drawn on the device by torch's seeded generator (only bit movement is
+checked there)."""
+import numpy as np
+import pytest
+import torch
+
+import long_context_sequence_gb300 as U
+import oracle as O
+import synthetic
+from gpu_helpers import assert_close, dev_bf16, empty_bf16, host_bits, host_f64
+
+pytestmark = pytest.mark.gpu
+
+H8B, G8B, D8B, HID8B = 32, 8, 128, 4096
+STD8B = 1.28   # std of x W^T for hidden 4096 and W ~ N(0, 0.02^2)
+
+
+def _gen(S, P, H, G, D, std):
+    q = synthetic.normal_bf16(0, synthetic.TENSOR_Q, (P, S, H // P, D), std=std)
+    k = synthetic.normal_bf16(0, synthetic.TENSOR_K, (P, S, G // P, D), std=std)
+    v = synthetic.normal_bf16(0, synthetic.TENSOR_V, (P, S, G // P, D), std=std)
+    return q, k, v
+
+
+def _check_fwd_rows(q, k, v, o, lse, rows, P, H, G, tag):
+    """Oracle on sampled rows of every rank/head group, against the GPU's o and lse."""
+    o_h, lse_h = host_f64(o), lse.cpu().double().numpy()
+    for r in range(P):
+        ro, rl = O.causal_attention_rows(synthetic.bf16_to_f64(q[r]), synthetic.bf16_to_f64(k[r]),
+                                         synthetic.bf16_to_f64(v[r]), rows)
+        assert_close(o_h[r][rows], ro, "%s o[rank %d]" % (tag, r))
+        assert_close(lse_h[r][:, rows], rl, "%s lse[rank %d]" % (tag, r))
+
+
+@pytest.mark.parametrize("S", [32768, 131072])
+def test_forward_8b_block_sampled_rows(S):
+    """8B-shaped head groups (P=8: 4 query heads, 1 KV head per rank) at S=32K and 128K;
+    512 sampled query rows per head at 128K (all heads of every rank)."""
+    P = 8
+    plan = U.ulysses_plan(U.make_config(S, P, HID8B, H8B, G8B, D8B))
+    q, k, v = _gen(S, P, H8B, G8B, D8B, STD8B)
+    o = empty_bf16((P, S, H8B // P, D8B))
+    lse = torch.empty((P, H8B // P, S), dtype=torch.float32, device="cuda")
+    U.ulysses_attn_fwd(plan, dev_bf16(q), dev_bf16(k), dev_bf16(v), o, lse)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    rows = synthetic.sample_rows(S, P, 512)
+    _check_fwd_rows(q, k, v, o, lse, rows, P, H8B, G8B, "S=%d" % S)
+
+
+def _bwd_check(S, P, H, G, D, std, n_rows, tail, tag):
+    plan = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
+    q, k, v = _gen(S, P, H, G, D, std)
+    do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D))
+    qg, kg, vg, dog = (dev_bf16(a) for a in (q, k, v, do))
+    o = empty_bf16((P, S, H // P, D))
+    lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
+    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse)
+    ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
+    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    rows = synthetic.sample_rows(S, P, n_rows)
+    dq_h, dk_h, dv_h = host_f64(dq), host_f64(dk), host_f64(dv)
+    ranks = range(P) if P <= 2 else (0, P // 2, P - 1)
+    for r in ranks:
+        qf, kf, vf, dof = (synthetic.bf16_to_f64(a[r]) for a in (q, k, v, do))
+        rdq, rdk, rdv = O.causal_attention_bwd_rows(qf, kf, vf, dof, rows, S - tail)
+        assert_close(dq_h[r][rows], rdq, "%s dq[rank %d] sampled rows" % (tag, r))
+        assert_close(dk_h[r][S - tail:], rdk, "%s dk[rank %d] tail keys" % (tag, r))
+        assert_close(dv_h[r][S - tail:], rdv, "%s dv[rank %d] tail keys" % (tag, r))
+    return plan
+
+
+def test_backward_8b_block_64k_sampled_rows():
+    """Training step of the 8B-shaped block at S=65536, P=8: dQ on sampled rows, dK/dV on
+    the last 256 keys (exact: only rows >= S-256 reach them), three ranks checked."""
+    _bwd_check(65536, 8, H8B, G8B, D8B, STD8B, 256, 256, "S=64K")
+
+
+def test_million_token_head_group_fwd_bwd():
+    """One rank's post-all-to-all share at S = 2^20: 4 query heads, 1 KV head, D=128,
+    Q/K/V ~ N(0,1) (a rotation of iid normals is again iid normal, so RoPE does not change
+    the draw); forward on 256 sampled rows, backward on sampled dQ rows and tail keys."""
+    S, P, H, G, D = 1 << 20, 1, 4, 1, 128
+    plan = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
+    q, k, v = _gen(S, P, H, G, D, 1.0)
+    o = empty_bf16((P, S, H, D))
+    lse = torch.empty((P, H, S), dtype=torch.float32, device="cuda")
+    qg, kg, vg = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    rows = synthetic.sample_rows(S, 8, 256)
+    _check_fwd_rows(q, k, v, o, lse, rows, P, H, G, "S=1M")
+    do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H, D))
+    ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
+    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dev_bf16(do), dq, dk, dv, ws)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    rows = synthetic.sample_rows(S, 8, 64)
+    qf, kf, vf, dof = (synthetic.bf16_to_f64(a[0]) for a in (q, k, v, do))
+    rdq, rdk, rdv = O.causal_attention_bwd_rows(qf, kf, vf, dof, rows, S - 64)
+    assert_close(host_f64(dq)[0][rows], rdq, "S=1M dq sampled rows")
+    assert_close(host_f64(dk)[0][S - 64:], rdk, "S=1M dk tail keys")
+    assert_close(host_f64(dv)[0][S - 64:], rdv, "S=1M dv tail keys")
+
+
+def test_full_hidden_permutes_million_tokens():
+    """seq->head and head->seq at S = 2^20, P=8, full hidden (32 q + 8 k + 8 v heads of 128),
+    12.9 GB each way: bit-exact round trip, and sampled tokens against the index formula
+    out[r2][s][h2] = in[s][r2*H/P + h2]."""
+    S, P, H, G, D = 1 << 20, 8, H8B, G8B, D8B
+    plan = U.ulysses_plan(U.make_config(S, P, HID8B, H, G, D))
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    x = torch.empty((S, H + 2 * G, D), dtype=torch.bfloat16, device="cuda")
+    for i in range(0, S, 1 << 17):   # in slices, to keep the fp32 temporary small
+        x[i:i + (1 << 17)] = torch.randn((min(1 << 17, S - i), H + 2 * G, D), generator=gen,
+                                         device="cuda").to(torch.bfloat16)
+    q, k, v = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, G // P, D)), empty_bf16((P, S, G // P, D))
+    U.ulysses_seq_to_head(plan, x, q, k, v)
+    back = empty_bf16((P, S // P, H, D))
+    U.ulysses_head_to_seq(plan, q, H, back)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    assert torch.equal(back.view(S, H, D), x[:, :H])
+    del back
+    bk = empty_bf16((P, S // P, G, D))
+    U.ulysses_head_to_seq(plan, k, G, bk)
+    torch.cuda.synchronize()
+    assert torch.equal(bk.view(S, G, D), x[:, H:H + G])
+    U.ulysses_head_to_seq(plan, v, G, bk)
+    torch.cuda.synchronize()
+    assert torch.equal(bk.view(S, G, D), x[:, H + G:])
+    del bk
+    toks = torch.from_numpy(synthetic.sample_rows(S, P, 64)).cuda()
+    xs = host_bits(x[toks])
+    hq, hk = H // P, G // P
+    qs, ks, vs = host_bits(q[:, toks]), host_bits(k[:, toks]), host_bits(v[:, toks])
+    for r2 in range(P):
+        for h2 in range(hq):
+            assert np.array_equal(qs[r2, :, h2], xs[:, r2 * hq + h2])
+        for h2 in range(hk):
+            assert np.array_equal(ks[r2, :, h2], xs[:, H + r2 * hk + h2])
+            assert np.array_equal(vs[r2, :, h2], xs[:, H + G + r2 * hk + h2])
+
+
+def test_rope_at_million_token_positions_sampled():
+    """RoPE at global positions up to 2^20 - 1 (theta 500000, D=128), sampled tokens against
+    the fp64 rotation of the same bf16 input (one q, one k, one v head keeps the draw small)."""
+    S, P, H, G, D, theta = 1 << 20, 1, 1, 1, D8B, 500000.0
+    plan = U.ulysses_plan(U.make_config(S, P, HID8B, H, G, D, rope_theta=theta))
+    x = synthetic.normal_bf16(0, synthetic.TENSOR_QKV, (S, H + 2 * G, D), std=STD8B)
+    q, k, v = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, G // P, D)), empty_bf16((P, S, G // P, D))
+    U.ulysses_seq_to_head(plan, dev_bf16(x), q, k, v, apply_rope=True)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    toks = synthetic.sample_rows(S, P, 256)
+    xf = synthetic.bf16_to_f64(x[toks])
+    rot = np.concatenate([O.apply_rope(xf[:, :H + G], toks, theta), xf[:, H + G:]], axis=1)
+    tg = torch.from_numpy(toks).cuda()
+    qs, ks = host_f64(q[:, tg]), host_f64(k[:, tg])
+    hq, hk = H // P, G // P
+    for r2 in range(P):
+        for h2 in range(hq):
+            ref = rot[:, r2 * hq + h2]
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+            assert np.all(np.abs(qs[r2, :, h2] - ref) <= ulp + 1e-5)
+        for h2 in range(hk):
+            ref = rot[:, H + r2 * hk + h2]
+            ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+            assert np.all(np.abs(ks[r2, :, h2] - ref) <= ulp + 1e-5)
