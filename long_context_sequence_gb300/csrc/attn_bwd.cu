@@ -9,17 +9,25 @@
 //
 // Three kernels:
 //   bwd_pre   D_i = rowsum(dO * O) in fp32 and zeroing of the fp32 dQ accumulator;
-//   bwd_main  one CTA per (rank, KV head, 128-key block), looping over the query heads of
-//             the group and the causally visible 128-row query tiles:
-//               S^T  = K Q_i^T, dP^T = V dO_i^T          (tcgen05, TMEM, M = keys)
-//               P^T, dS^T per key row on 4 warps -> TMEM (bf16) and dS -> smem
-//               dV += P^T dO_i, dK += dS^T Q_i           (A operand from TMEM)
-//               dQ_i = dS K -> TMEM -> fp32 vector reductions into the accumulator;
+//   bwd_main  one CTA per (rank, KV head, 128-key block).  Work items are (64-row query
+//             tile, query head of the group) pairs from the diagonal on.  Two items are in
+//             flight in two TMEM regions, so one item's tensor work overlaps the other's
+//             element-wise work:
+//               MMA1:  S^T = K Q^T, dP^T = V dO^T      (bf16, M = 128 keys, N = 64 rows)
+//               warps 0-3 / 4-7 (one group per region, thread = key row):
+//                      P^T = exp2(S^T * scale*log2e - lse*log2e) -> TMEM (fp16),
+//                      dS = P (dP - D) -> smem (fp16, 128-byte swizzle),
+//                      Q and dO tiles converted in place to fp16;
+//               MMA2:  dQ^T = K^T dS^T                  (M = 128 = d, TMEM over dP^T),
+//                      dV += P^T dO, dK += dS^T Q       (fp32 accumulators in TMEM);
+//               warps 8-11 (thread = d): dQ^T -> coalesced fp32 reductions into the
+//                      workspace accumulator (lanes are consecutive d of one row);
 //   bwd_dq    fp32 dQ accumulator -> bf16.
-// dS is kept as hi + lo bf16 parts for dK (hi in the smem tile that also feeds dQ, lo in
-// TMEM), so the long dK sums see dS to ~16 bits.
-// TMEM (512 columns): S^T [0,128) (P^T bf16 over [0,64)), dP^T [128,256) (dS^T lo part,
-// bf16, over [128,192)), dV [256,256+D), dK [256+D,256+2D); dQ goes to [64,128), [192,256).
+// The second MMA group uses fp16 operands (P in [0,1], dS, dO, Q and an fp16 copy of K,
+// all clamped to the finite fp16 range): with the same tensor rate, fp16 keeps 11
+// significand bits against bf16's 8, which the long dK/dQ sums need.
+// TMEM (512 columns): region X in {0,1} at 128X: S^T [0,64) -> P^T [0,32); dP^T [64,128)
+// -> dQ^T [64,128).  dV at [256, 256+D), dK at [256+D, 256+2D).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -28,24 +36,27 @@
 namespace uly {
 namespace {
 
-constexpr int BM = 128;  // query rows per item
-constexpr int BN = 128;  // keys per CTA
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4, kMmaWarp = 5;
+constexpr int BN = 128;   // keys per CTA (TMEM lanes of S^T, dP^T, dV, dK)
+constexpr int BMI = 64;   // query rows per item
+constexpr int NST = 3;    // Q/dO stages
+constexpr int kThreads = 448;
+constexpr int kDqWarp0 = 8, kTmaWarp = 12, kMmaWarp = 13;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kBox = 128 * 64 * 2;
+constexpr int kBox128 = 128 * 128;   // [128 rows][128 bytes]
+constexpr int kBox64 = 64 * 128;     // [64 rows][128 bytes]
 
 template <int D>
 struct BwdLayout {
-  static constexpr int kTile = (D / 64) * kBox;   // [128][D] bf16
+  static constexpr int kKV = (D / 64) * kBox128;   // K or V tile [128][D] bf16
+  static constexpr int kItem = (D / 64) * kBox64;  // Q or dO item [64][D]
   static constexpr int kK = 0;
-  static constexpr int kV = kTile;
-  static constexpr int kQ = 2 * kTile;             // [2] stages
-  static constexpr int kDO = 4 * kTile;            // [2] stages
-  static constexpr int kDS = 6 * kTile;            // [128 keys][128 q] bf16 = 2 boxes
-  static constexpr int kDSBytes = 2 * kBox;
-  static constexpr int kRow = kDS + kDSBytes;      // lse2[2][128], delta[2][128] fp32
-  static constexpr int kBar = kRow + 4 * 128 * 4;
+  static constexpr int kV = kKV;
+  static constexpr int kK16 = 2 * kKV;             // fp16 copy of K as two 64-column atoms
+  static constexpr int kQ = kK16 + 2 * kBox128;    // [NST]
+  static constexpr int kDO = kQ + NST * kItem;     // [NST]
+  static constexpr int kDS = kDO + NST * kItem;    // [2] fp16 [128 keys][64 q]
+  static constexpr int kRow = kDS + 2 * kBox128;   // [2 groups][2][128] fp32: lse2 | delta
+  static constexpr int kBar = kRow + 2 * 2 * 128 * 4;
   static constexpr int kBytes = kBar + 256;
 };
 
@@ -61,10 +72,16 @@ struct BwdArgs {
   uint64_t limit_ns;
 };
 
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
-               "f"(c), "f"(d)
-               : "memory");
+__device__ __forceinline__ void red_add(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// Item -> (first query row, local query head).  Items run over the 64-row query tiles
+// that see this key block (from the diagonal on) and, within a tile, the group's heads.
+__device__ __forceinline__ void item_coords(int it, int nb, int gg, int group, int& q0, int& hh) {
+  const int qi = it / group;
+  q0 = nb * BN + qi * BMI;
+  hh = gg * group + (it - qi * group);
 }
 
 template <int D>
@@ -78,18 +95,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) atomicCAS(a.status, kOk, kErrUnsupported);
     return;
   }
-  float* lse_s = reinterpret_cast<float*>(smem + L::kRow);   // [2][128]
-  float* dlt_s = lse_s + 256;                                  // [2][128]
+  float* rowterms = reinterpret_cast<float*>(smem + L::kRow);   // [group X][u&1][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qd_full = bars + 1;    // [2]
-  uint64_t* qd_empty = bars + 3;   // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* dq_full = bars + 7;
-  uint64_t* dq_free = bars + 8;
-  uint64_t* drain = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
+  uint64_t* qd_full = bars + 1;              // [NST]
+  uint64_t* qd_empty = bars + 1 + NST;       // [NST]
+  uint64_t* s_full = bars + 1 + 2 * NST;     // [2] per TMEM region
+  uint64_t* p_full = s_full + 2;             // [2]
+  uint64_t* dq_full = p_full + 2;            // [2]
+  uint64_t* dq_free = dq_full + 2;           // [2]
+  uint64_t* k16_ready = dq_free + 2;
+  uint64_t* acc_done = k16_ready + 1;
+  uint64_t* drain = acc_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -97,20 +115,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r = blockIdx.x / per_rank;
   const int rem = blockIdx.x - r * per_rank;
   const int gg = rem / a.nkb;
-  const int nb = rem - gg * a.nkb;           // key block; nb = 0 (most work) first
-  const int nq = (a.S + BM - 1) / BM;
-  const int n_items = a.group * (nq - nb);   // (query tile, head of the group) pairs
+  const int nb = rem - gg * a.nkb;                         // key block; 0 (most work) first
+  const int nqi = (a.S - nb * BN + BMI - 1) / BMI;         // 64-row query tiles that see it
+  const int n_items = a.group * nqi;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 128);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 128);
+      mbar_init(&dq_full[i], 1);
+      mbar_init(&dq_free[i], 128);
+    }
+    mbar_init(k16_ready, 128);
+    mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -131,205 +153,240 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * L::kTile);
+      mbar_arrive_expect_tx(kv_full, 2 * L::kKV);
       for (int b = 0; b < D / 64; ++b) {
-        tma_load_4d(smem + L::kK + b * kBox, &tm_k, kv_full, 64 * b, gg, nb * BN, r);
-        tma_load_4d(smem + L::kV + b * kBox, &tm_v, kv_full, 64 * b, gg, nb * BN, r);
+        tma_load_4d(smem + L::kK + b * kBox128, &tm_k, kv_full, 64 * b, gg, nb * BN, r);
+        tma_load_4d(smem + L::kV + b * kBox128, &tm_v, kv_full, 64 * b, gg, nb * BN, r);
       }
       int issued = 0;
       for (int it = 0; it < n_items; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        const int i = nb + it / a.group;
-        const int hh = gg * a.group + it % a.group;
-        if (it >= 2 && !mbar_wait(&qd_empty[st], ph ^ 1, wc)) break;
-        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kTile);
+        const int st = it % NST;
+        const uint32_t ph = (it / NST) & 1;
+        int q0, hh;
+        item_coords(it, nb, gg, a.group, q0, hh);
+        if (it >= NST && !mbar_wait(&qd_empty[st], ph ^ 1, wc)) break;
+        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kItem);
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_4d(smem + L::kQ + st * L::kTile + b * kBox, &tm_q, &qd_full[st], 64 * b, hh,
-                      i * BM, r);
-          tma_load_4d(smem + L::kDO + st * L::kTile + b * kBox, &tm_do, &qd_full[st], 64 * b,
-                      hh, i * BM, r);
+          tma_load_4d(smem + L::kQ + st * L::kItem + b * kBox64, &tm_q, &qd_full[st], 64 * b,
+                      hh, q0, r);
+          tma_load_4d(smem + L::kDO + st * L::kItem + b * kBox64, &tm_do, &qd_full[st], 64 * b,
+                      hh, q0, r);
         }
         ++issued;
       }
       mbar_drain(kv_full, 0, a.limit_ns);
-      for (int it = issued > 2 ? issued - 2 : 0; it < issued; ++it)
-        mbar_drain(&qd_full[it & 1], (it >> 1) & 1, a.limit_ns);
+      for (int it = issued > NST ? issued - NST : 0; it < issued; ++it)
+        mbar_drain(&qd_full[it % NST], (it / NST) & 1, a.limit_ns);
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(BN, BM, false, false);   // M keys, N q
-      constexpr uint32_t idesc_kv = idesc_bf16(BN, D, false, true);    // A tmem, B MN-major
-      constexpr uint32_t idesc_q = idesc_bf16(BM, 64, true, true);     // dS, K both MN-major
+      // S^T, dP^T: M = keys, N = 64 query rows, K = D; bf16, both K-major.
+      constexpr uint32_t id_s = idesc_bf16(BN, BMI, false, false);
+      // dV += P^T dO, dK += dS^T Q: M = keys, N = D, K = 64 rows; fp16, B MN-major.
+      constexpr uint32_t id_kv_t = idesc_f16(BN, D, false, true);   // A = P^T from TMEM
+      constexpr uint32_t id_kv_s = idesc_f16(BN, D, false, true);   // A = dS smem, K-major
+      // dQ^T = K^T dS^T: M = 128 (d, zero-padded when D = 64), N = 64 rows, K = 128 keys.
+      constexpr uint32_t id_q = idesc_f16(128, BMI, true, true);
       const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
-      const uint32_t sDS = smem_u32(smem + L::kDS);
+      const uint32_t sK16 = smem_u32(smem + L::kK16);
       bool alive = mbar_wait(kv_full, 0, wc);
-      for (int it = 0; alive && it < n_items; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kTile);
-        const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kTile);
-        if (!mbar_wait(&qd_full[st], ph, wc)) break;
-        if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, wc)) break;
-        tc_fence_after();
+      auto mma1 = [&](int it) {
+        const int X = it & 1, st = it % NST;
+        const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kItem);
+        const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kItem);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
-          mma_ss(tbase + 0, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ + off, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t offa = (kk / 4) * kBox128 + (kk % 4) * 32;
+          const uint32_t offb = (kk / 4) * kBox64 + (kk % 4) * 32;
+          mma_ss(tbase + 128 * X, sdesc_sw128(sK + offa, 16, 1024),
+                 sdesc_sw128(sQ + offb, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
-          mma_ss(tbase + 128, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t offa = (kk / 4) * kBox128 + (kk % 4) * 32;
+          const uint32_t offb = (kk / 4) * kBox64 + (kk % 4) * 32;
+          mma_ss(tbase + 128 * X + 64, sdesc_sw128(sV + offa, 16, 1024),
+                 sdesc_sw128(sDO + offb, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, it & 1, wc)) break;
+        mma_commit(&s_full[X]);
+      };
+      auto mma2 = [&](int it) -> bool {
+        const int X = it & 1, st = it % NST;
+        if (!mbar_wait(&p_full[X], (it >> 1) & 1, wc)) return false;
+        if (it == 0 && !mbar_wait(k16_ready, 0, wc)) return false;
         tc_fence_after();
+        const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kItem);     // fp16 by now
+        const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kItem);   // fp16 by now
+        const uint32_t sDS = smem_u32(smem + L::kDS + X * kBox128);
+        // dQ^T first, so its read-out overlaps the dV/dK MMAs
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tbase + 256, tbase + 0 + kk * 8, sdesc_sw128(sDO + kk * 2048, kBox, 1024),
-                 idesc_kv, (it > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q with dS = hi + lo: hi from the smem tile (K-major A operand),
-        // lo from TMEM, so dK sees dS to about 16 bits instead of 8.
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tbase + 128 * X + 64, sdesc_sw128(sK16 + kk * 2048, kBox128, 1024),
+                 sdesc_sw128(sDS + kk * 2048, kBox128, 1024), id_q, kk > 0 ? 1u : 0u);
+        mma_commit(&dq_full[X]);
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ss(tbase + 256 + D, sdesc_sw128(sDS + (kk / 4) * kBox + (kk % 4) * 32, 16, 1024),
-                 sdesc_sw128(sQ + kk * 2048, kBox, 1024), idesc_kv,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BMI / 16; ++kk)
+          mma_ts(tbase + 256, tbase + 128 * X + kk * 8, sdesc_sw128(sDO + kk * 2048, kBox64, 1024),
+                 id_kv_t, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tbase + 256 + D, tbase + 128 + kk * 8, sdesc_sw128(sQ + kk * 2048, kBox, 1024),
-                 idesc_kv, 1u);
-#pragma unroll
-        for (int half = 0; half < D / 64; ++half)
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tbase + (half ? 192 : 64), sdesc_sw128(sDS + kk * 2048, kBox, 1024),
-                   sdesc_sw128(sK + half * kBox + kk * 2048, kBox, 1024), idesc_q,
-                   kk > 0 ? 1u : 0u);
-        mma_commit(dq_full);
+        for (int kk = 0; kk < BMI / 16; ++kk)
+          mma_ss(tbase + 256 + D, sdesc_sw128(sDS + kk * 32, 16, 1024),
+                 sdesc_sw128(sQ + kk * 2048, kBox64, 1024), id_kv_s, (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&qd_empty[st]);
+        return true;
+      };
+      for (int it = 0; alive && it < n_items; ++it) {
+        const int X = it & 1, st = it % NST;
+        if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) { alive = false; break; }
+        if (it >= 2 && !mbar_wait(&dq_free[X], ((it - 2) >> 1) & 1, wc)) { alive = false; break; }
+        tc_fence_after();
+        mma1(it);
+        if (it >= 1 && !mma2(it - 1)) { alive = false; break; }
       }
+      if (alive && n_items > 0 && mma2(n_items - 1)) mma_commit(acc_done);
       mma_commit(drain);
       mbar_drain(drain, 0, a.limit_ns);
     }
-  } else {
-    // Compute warpgroup: thread = key row (TMEM lane) for S^T/dP^T, = query row for dQ.
-    const int row = warp * 32 + lane;
-    const int key_g = nb * BN + row;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const float sl2 = a.scale_log2;
-    uint8_t* sDS = smem + L::kDS;
-    bool ok = true;
-    for (int it = 0; it < n_items; ++it) {
-      const int i = nb + it / a.group;
-      const int hh = gg * a.group + it % a.group;
-      const int q_g = i * BM + row;              // this thread's query column / dQ row
-      float* lse_b = lse_s + (it & 1) * 128;
-      float* dlt_b = dlt_s + (it & 1) * 128;
-      const size_t rowterm = ((size_t)r * a.hl + hh) * a.S + q_g;
-      lse_b[row] = q_g < a.S ? a.lse[rowterm] * 1.4426950408889634f : INFINITY;
-      dlt_b[row] = q_g < a.S ? a.delta[rowterm] : 0.f;
-      named_bar_sync(1, 128);
-      ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, wc));
-      if (!ok) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dp[32];
-        tmem_ld32(tbase + lane_off + 32 * c, sv);
-        tmem_ld32(tbase + lane_off + 128 + 32 * c, dp);
-        uint32_t pk[16], dk[16], lo[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int ql = 32 * c + 2 * u + e;
-            const int qg = i * BM + ql;
-            const bool valid = key_g <= qg && qg < a.S && key_g < a.S;
-            const float p = valid ? ex2_approx(fmaf(__uint_as_float(sv[2 * u + e]), sl2, -lse_b[ql]))
-                                  : 0.f;
-            pv[e] = p;
-            dv[e] = p * (__uint_as_float(dp[2 * u + e]) - dlt_b[ql]);
-          }
-          pk[u] = pack_bf16x2(pv[0], pv[1]);
-          dk[u] = pack_bf16x2(dv[0], dv[1]);          // dS rounded to bf16 (hi part)
-          const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&dk[u]);
-          const float2 hf = __bfloat1622float2(hi);
-          lo[u] = pack_bf16x2(dv[0] - hf.x, dv[1] - hf.y);   // what the rounding lost
-        }
-        tmem_st16(tbase + lane_off + 16 * c, pk);
-        tmem_st16(tbase + lane_off + 128 + 16 * c, lo);
-        // dS tile in smem: [key row][q], 64-column atoms of 128-byte swizzled rows.
-        uint8_t* atom = sDS + (c / 2) * kBox + row * 128;
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int chunk = (c % 2) * 4 + u;
-          uint4 v = make_uint4(dk[4 * u], dk[4 * u + 1], dk[4 * u + 2], dk[4 * u + 3]);
-          *reinterpret_cast<uint4*>(atom + ((chunk ^ (row & 7)) * 16)) = v;
-        }
+  } else if (warp >= kDqWarp0) {
+    // dQ warpgroup: thread = d (TMEM lane of dQ^T).  First the fp16 copy of K.
+    const int d = (warp - kDqWarp0) * 32 + lane;
+    bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, wc));
+    if (ok) {
+      uint8_t* k16 = smem + L::kK16;
+      for (int c = d; c < 2 * kBox128 / 16; c += 128) {
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (c * 16 < L::kKV)
+          v = bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(smem + L::kK + c * 16));
+        *reinterpret_cast<uint4*>(k16 + c * 16) = v;
       }
-      tmem_st_wait();
       fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(p_full);
-      ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wc));
+    }
+    mbar_arrive(k16_ready);
+    const uint32_t lane_off = (uint32_t)((warp - kDqWarp0) * 32) << 16;
+    const bool active = (warp - kDqWarp0) * 32 < D;      // warp-uniform
+    for (int it = 0; ok && it < n_items; ++it) {
+      const int X = it & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[X], (it >> 1) & 1, wc));
       if (!ok) break;
       tc_fence_after();
-      float* dq_row = a.dq_acc + (((size_t)r * a.S + q_g) * a.hl + hh) * D;
-#pragma unroll 1
-      for (int half = 0; half < D / 64; ++half) {
+      if (active) {
+        int q0, hh;
+        item_coords(it, nb, gg, a.group, q0, hh);
+        float* base = a.dq_acc + (((size_t)r * a.S + q0) * a.hl + hh) * D + d;
+        const size_t row_stride = (size_t)a.hl * D;
 #pragma unroll 1
         for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t v[32];
-          tmem_ld32(tbase + lane_off + (half ? 192 : 64) + 32 * c2, v);
-          if (q_g < a.S) {
-            float* dst = dq_row + half * 64 + c2 * 32;
+          tmem_ld32(tbase + lane_off + 128 * X + 64 + 32 * c2, v);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              red_add_v4(dst + 4 * j, __uint_as_float(v[4 * j]) * a.scale,
-                         __uint_as_float(v[4 * j + 1]) * a.scale,
-                         __uint_as_float(v[4 * j + 2]) * a.scale,
-                         __uint_as_float(v[4 * j + 3]) * a.scale);
+          for (int j = 0; j < 32; ++j) {
+            const int qc = 32 * c2 + j;
+            if (q0 + qc < a.S) red_add(base + qc * row_stride, __uint_as_float(v[j]) * a.scale);
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(dq_free);
+      mbar_arrive(&dq_free[X]);
     }
-    // dK, dV of this key block (complete: the last dq_full covered every MMA).
-    if (ok && n_items > 0) {
+  } else {
+    // Compute warpgroups: group X handles items X, X+2, ...; thread = key row.
+    const int X = warp / 4;
+    const int row = (warp % 4) * 32 + lane;
+    const int t128 = threadIdx.x % 128;
+    const int key_g = nb * BN + row;
+    const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
+    const uint32_t ts = tbase + lane_off + 128 * X;   // S^T, then P^T
+    const uint32_t tp = ts + 64;                       // dP^T
+    const float sl2 = a.scale_log2;
+    uint8_t* sDS = smem + L::kDS + X * kBox128 + row * 128;
+    bool ok = true;
+    for (int it = X; it < n_items; it += 2) {
+      const int u = it >> 1, st = it % NST;
+      int q0, hh;
+      item_coords(it, nb, gg, a.group, q0, hh);
+      float* terms = rowterms + (X * 2 + (u & 1)) * 128;   // [0,64) lse2, [64,128) delta
+      {
+        const int qc = t128 & 63;
+        const int qg = q0 + qc;
+        const size_t idx = ((size_t)r * a.hl + hh) * a.S + qg;
+        if (t128 < 64)
+          terms[t128] = qg < a.S ? a.lse[idx] * 1.4426950408889634f : INFINITY;
+        else
+          terms[t128] = qg < a.S ? a.delta[idx] : 0.f;
+      }
+      named_bar_sync(1 + X, 128);
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], u & 1, wc));
+      if (!ok) break;
       tc_fence_after();
-      const size_t out_off = (((size_t)r * a.S + key_g) * a.gl + gg) * D;
+      const bool need_mask = (q0 < nb * BN + BN) || (q0 + BMI > a.S) || (nb * BN + BN > a.S);
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        __nv_bfloat16* dst = (which ? a.dk : a.dv) + out_off;
-        const float mul = which ? a.scale : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tbase + lane_off + 256 + which * D + 32 * c, v);
-          if (key_g < a.S) {
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(ts + 32 * c, sv);
+        tmem_ld32(tp + 32 * c, dp);
+        uint32_t pk[16], dk[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint4 o;
-              o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * mul, __uint_as_float(v[8 * j + 1]) * mul);
-              o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * mul, __uint_as_float(v[8 * j + 3]) * mul);
-              o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * mul, __uint_as_float(v[8 * j + 5]) * mul);
-              o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * mul, __uint_as_float(v[8 * j + 7]) * mul);
-              *reinterpret_cast<uint4*>(dst + 32 * c + 8 * j) = o;
-            }
+        for (int i2 = 0; i2 < 16; ++i2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int qc = 32 * c + 2 * i2 + e;
+            float p = ex2_approx(fmaf(__uint_as_float(sv[2 * i2 + e]), sl2, -terms[qc]));
+            if (need_mask && !(key_g <= q0 + qc && q0 + qc < a.S && key_g < a.S)) p = 0.f;
+            pv[e] = p;
+            dv[e] = p * (__uint_as_float(dp[2 * i2 + e]) - terms[64 + qc]);
           }
+          pk[i2] = pack_f16x2_sat(pv[0], pv[1]);
+          dk[i2] = pack_f16x2_sat(dv[0], dv[1]);
+        }
+        tmem_st16(ts + 16 * c, pk);                     // P^T (fp16) over S^T
+#pragma unroll
+        for (int u4 = 0; u4 < 4; ++u4) {                // dS row, 128-byte swizzle
+          const int chunk = c * 4 + u4;
+          *reinterpret_cast<uint4*>(sDS + ((chunk ^ (row & 7)) * 16)) =
+              make_uint4(dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
         }
       }
-    } else if (ok && key_g < a.S) {
-      // No visible query rows (cannot happen for key_g < S, kept for safety): zero grads.
-      for (int d = 0; d < D; ++d) {
-        a.dk[(((size_t)r * a.S + key_g) * a.gl + gg) * D + d] = __float2bfloat16_rn(0.f);
-        a.dv[(((size_t)r * a.S + key_g) * a.gl + gg) * D + d] = __float2bfloat16_rn(0.f);
+      // The item's Q and dO tiles are no longer needed in bf16 (S^T, dP^T are done):
+      // convert them in place to fp16 for dK and dV.
+      {
+        uint8_t* q16 = smem + L::kQ + st * L::kItem;
+        uint8_t* do16 = smem + L::kDO + st * L::kItem;
+#pragma unroll 1
+        for (int cidx = t128; cidx < L::kItem / 16; cidx += 128) {
+          uint4* pq = reinterpret_cast<uint4*>(q16 + cidx * 16);
+          uint4* pd = reinterpret_cast<uint4*>(do16 + cidx * 16);
+          const uint4 vq = *pq, vd = *pd;
+          *pq = bf16x8_to_f16x8(vq);
+          *pd = bf16x8_to_f16x8(vd);
+        }
+      }
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&p_full[X]);
+    }
+    // dV (group 0) and dK (group 1) of this key block, once every MMA has finished.
+    if (ok && n_items > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, wc));
+    if (ok && n_items > 0) {
+      tc_fence_after();
+      __nv_bfloat16* dst = (X ? a.dk : a.dv) + (((size_t)r * a.S + key_g) * a.gl + gg) * D;
+      const float mul = X ? a.scale : 1.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tbase + lane_off + 256 + X * D + 32 * c, v);
+        if (key_g < a.S) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * mul, __uint_as_float(v[8 * j + 1]) * mul);
+            o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * mul, __uint_as_float(v[8 * j + 3]) * mul);
+            o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * mul, __uint_as_float(v[8 * j + 5]) * mul);
+            o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * mul, __uint_as_float(v[8 * j + 7]) * mul);
+            *reinterpret_cast<uint4*>(dst + 32 * c + 8 * j) = o;
+          }
+        }
       }
     }
   }
@@ -422,8 +479,8 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)hl * D * 2, (uint64_t)p.S * hl * D * 2};
   const uint64_t dk4[4] = {(uint64_t)D, (uint64_t)gl, (uint64_t)p.S, (uint64_t)p.P};
   const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)gl * D * 2, (uint64_t)p.S * gl * D * 2};
-  if (!make_tmap_4d_bf16(&tq, q, dq4, sq, 64, BM, &err) ||
-      !make_tmap_4d_bf16(&tdo, d_o, dq4, sq, 64, BM, &err) ||
+  if (!make_tmap_4d_bf16(&tq, q, dq4, sq, 64, BMI, &err) ||
+      !make_tmap_4d_bf16(&tdo, d_o, dq4, sq, 64, BMI, &err) ||
       !make_tmap_4d_bf16(&tk, k, dk4, sk, 64, BN, &err) ||
       !make_tmap_4d_bf16(&tv, v, dk4, sk, 64, BN, &err))
     return cudaErrorInvalidValue;

@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace uly {
 
@@ -159,6 +160,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          ((uint32_t)(M >> 4) << 24);
 }
 
+// The same for fp16 A/B (formats 0), fp32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major,
+                                                 bool b_mn_major) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.  Bits: [0,14) address >> 4,
 // [16,30) leading byte offset >> 4, [32,46) stride byte offset >> 4, [46,48) = 1
 // (descriptor version of tcgen05), [61,64) layout (2 = 128-byte swizzle).
@@ -251,6 +259,24 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// fp16 pair, round to nearest even, clamped to the finite fp16 range.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  lo = fminf(fmaxf(lo, -65504.f), 65504.f);
+  hi = fminf(fmaxf(hi, -65504.f), 65504.f);
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+// 8 bf16 -> 8 fp16 (16 bytes in, 16 bytes out).
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
+  uint4 o;
+  float2 f;
+  f = __bfloat1622float2(b[0]); o.x = pack_f16x2_sat(f.x, f.y);
+  f = __bfloat1622float2(b[1]); o.y = pack_f16x2_sat(f.x, f.y);
+  f = __bfloat1622float2(b[2]); o.z = pack_f16x2_sat(f.x, f.y);
+  f = __bfloat1622float2(b[3]); o.w = pack_f16x2_sat(f.x, f.y);
+  return o;
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
