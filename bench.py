@@ -211,6 +211,7 @@ def run_ours(args):
     qkv = torch.empty(sh["qkv"], dtype=bf, device=dev)
     q, k, v = (torch.empty(sh[n], dtype=bf, device=dev) for n in ("q", "k", "v"))
     o = torch.empty(sh["o"], dtype=bf, device=dev)
+    o_lo = torch.empty(sh["o"], dtype=bf, device=dev)
     lse = torch.empty(sh["lse"], dtype=torch.float32, device=dev)
     o_seq = torch.empty(sh["o_seq"], dtype=bf, device=dev)
     do = torch.empty(sh["o"], dtype=bf, device=dev)
@@ -234,13 +235,13 @@ def run_ours(args):
         mark(1)
         U.ulysses_seq_to_head(plan, qkv, q, k, v, apply_rope=True, stream=sid)
         mark(2)
-        U.ulysses_attn_fwd(plan, q, k, v, o, lse, sid)
+        U.ulysses_attn_fwd(plan, q, k, v, o, lse, sid, o_lo=o_lo)
         mark(3)
         U.ulysses_head_to_seq(plan, o, H, o_seq, sid)
         mark(4)
         U.ulysses_seq_to_head_heads(plan, do_seq, H, do, sid)
         mark(5)
-        U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid)
+        U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid, o_lo=o_lo)
         mark(6)
         U.ulysses_head_to_seq(plan, dq, H, dq_seq, sid)
         U.ulysses_head_to_seq(plan, dk, G, dk_seq, sid)

@@ -122,19 +122,24 @@ uly_status ulysses_seq_to_head_heads(uly_plan plan, const void *x_seq, int n_hea
  * compute its share using standard FlashAttention locally", Ulysses-trick page para 2;
  * tiled so no S x S matrix is ever stored, Hugging Face post para 3).  For query head
  * h' of rank r (KV head h' / (H/G)):  o = softmax(scale * q k^T, causal) v in bf16 with
- * fp32 softmax and accumulation; lse = natural-log logsumexp of the scaled scores. */
+ * fp32 softmax and accumulation; lse = natural-log logsumexp of the scaled scores.
+ * o_lo (optional, may be NULL; layout of o): receives bf16(O - o), what the bf16 rounding
+ * of each output element dropped.  Passing it on to ulysses_attn_bwd lets the backward
+ * form its row terms dO.O from O to ~16 significant bits instead of 8. */
 uly_status ulysses_attn_fwd(uly_plan plan, const void *q, const void *k, const void *v,
-                            void *o, float *lse, void *stream);
+                            void *o, void *o_lo, float *lse, void *stream);
 
 /* Backward of ulysses_attn_fwd for the training step (Hugging Face post para 1: the
- * method is for training).  Inputs q, k, v, o, lse as above and the upstream gradient
- * d_o in head layout [P][S][H/P][D].  Outputs dq [P][S][H/P][D], dk, dv [P][S][G/P][D]
- * in bf16; dk and dv sum the contributions of all query heads of a KV head.
+ * method is for training).  Inputs q, k, v, o, lse as above, o_lo from the forward (or
+ * NULL: the row terms then use the bf16 o alone) and the upstream gradient d_o in head
+ * layout [P][S][H/P][D].  Outputs dq [P][S][H/P][D], dk, dv [P][S][G/P][D] in bf16; dk
+ * and dv sum the contributions of all query heads of a KV head.
  * workspace: ulysses_workspace_bytes(plan) bytes of device memory (fp32 accumulators);
  * its contents on entry do not matter. */
 uly_status ulysses_attn_bwd(uly_plan plan, const void *q, const void *k, const void *v,
-                            const void *o, const float *lse, const void *d_o, void *dq,
-                            void *dk, void *dv, void *workspace, void *stream);
+                            const void *o, const void *o_lo, const float *lse,
+                            const void *d_o, void *dq, void *dk, void *dv, void *workspace,
+                            void *stream);
 
 /* head->seq all-to-all, the inverse of seq->head ("another all-to-all operation reverses
  * the redistribution", Hugging Face post para 5): x_head [P][S][n_heads/P][D] ->

@@ -70,8 +70,8 @@ def load_library(path: str = LIB_PATH):
         "ulysses_qkv_proj": ([vp, vp, vp, vp, vp], i32),
         "ulysses_seq_to_head": ([vp, vp, i32, i32, vp, vp, vp, vp], i32),
         "ulysses_seq_to_head_heads": ([vp, vp, i32, vp, vp], i32),
-        "ulysses_attn_fwd": ([vp, vp, vp, vp, vp, vp, vp], i32),
-        "ulysses_attn_bwd": ([vp] * 12, i32),
+        "ulysses_attn_fwd": ([vp] * 8, i32),
+        "ulysses_attn_bwd": ([vp] * 13, i32),
         "ulysses_head_to_seq": ([vp, vp, i32, vp, vp], i32),
         "ulysses_sync_status": ([vp, vp], i32),
         "ulysses_bytes_moved": ([vp], u64),
@@ -174,15 +174,17 @@ def ulysses_seq_to_head_heads(plan, x_seq, n_heads, x_head, stream=None):
                                                     _ptr(x_head), _stream(stream)))
 
 
-def ulysses_attn_fwd(plan, q, k, v, o, lse, stream=None):
+def ulysses_attn_fwd(plan, q, k, v, o, lse, stream=None, o_lo=None):
     _check(load_library().ulysses_attn_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
-                                           _ptr(lse), _stream(stream)))
+                                           _ptr(o_lo), _ptr(lse), _stream(stream)))
 
 
-def ulysses_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, stream=None):
+def ulysses_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, stream=None,
+                     o_lo=None):
     _check(load_library().ulysses_attn_bwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o),
-                                           _ptr(lse), _ptr(d_o), _ptr(dq), _ptr(dk), _ptr(dv),
-                                           _ptr(workspace), _stream(stream)))
+                                           _ptr(o_lo), _ptr(lse), _ptr(d_o), _ptr(dq),
+                                           _ptr(dk), _ptr(dv), _ptr(workspace),
+                                           _stream(stream)))
 
 
 def ulysses_head_to_seq(plan, x_head, n_heads, x_seq, stream=None):

@@ -305,28 +305,30 @@ uly_status ulysses_head_to_seq(uly_plan plan, const void* x_head, int n_heads, v
 }
 
 uly_status ulysses_attn_fwd(uly_plan plan, const void* q, const void* k, const void* v, void* o,
-                            float* lse, void* stream) {
+                            void* o_lo, float* lse, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = plan->p;
   if (p.S == 0) return ULY_OK;
   if (!q || !k || !v || !o || !lse) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(o_lo))
     return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  return launched(uly::launch_attn_fwd(p, q, k, v, o, lse, as_stream(stream)), "attn_fwd launch");
+  return launched(uly::launch_attn_fwd(p, q, k, v, o, o_lo, lse, as_stream(stream)),
+                  "attn_fwd launch");
 }
 
 uly_status ulysses_attn_bwd(uly_plan plan, const void* q, const void* k, const void* v,
-                            const void* o, const float* lse, const void* d_o, void* dq, void* dk,
-                            void* dv, void* workspace, void* stream) {
+                            const void* o, const void* o_lo, const float* lse, const void* d_o,
+                            void* dq, void* dk, void* dv, void* workspace, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = plan->p;
   if (p.S == 0) return ULY_OK;
   if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace)
     return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
-  const void* ptrs[] = {q, k, v, o, lse, d_o, dq, dk, dv, workspace};
+  const void* ptrs[] = {q, k, v, o, o_lo, lse, d_o, dq, dk, dv, workspace};
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  return launched(uly::launch_attn_bwd(p, q, k, v, o, lse, d_o, dq, dk, dv, workspace,
+  return launched(uly::launch_attn_bwd(p, q, k, v, o, o_lo, lse, d_o, dq, dk, dv, workspace,
                                        as_stream(stream)),
                   "attn_bwd launch");
 }

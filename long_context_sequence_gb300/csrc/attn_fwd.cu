@@ -11,12 +11,11 @@
 //     and neighbouring blocks are the query heads of one KV head, so K/V stay in L2;
 //   * warp 8 (TMA): Q0/Q1 once, then K_j and V_j into a 2-deep ring (128-byte swizzle);
 //   * warp 9 (MMA, one thread): S_t = Q_t K_j^T into TMEM (fp32, 128 columns each), then
-//     O_t += P_t V_j with P_t read from TMEM (fp16, written over S_t; P <= 2^8 with the
-//     lazy rescale below) and V_j converted to fp16 in place by warps 10-11, so the
-//     weights keep 11 significand bits;
+//     O_t += P_t V_j with P_t read from TMEM (bf16, written over S_t);
 //   * warps 0-3 / 4-7: the online softmax of Q0 / Q1, one thread per row (= TMEM lane),
 //     in the log2 domain, with lazy rescaling of O (only when the running max grows by
-//     more than 2^8); they also write O / l and lse at the end;
+//     more than 2^8); they also write O / l (bf16), optionally its bf16 rounding residual
+//     (so a backward pass can form dO.O to ~16 bits), and lse at the end;
 //   * causal tile skipping: Q0 sees KV tiles 0..m0/128, Q1 one more.
 // TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D) of 512 columns.
 #include <cuda_bf16.h>
@@ -28,8 +27,8 @@ namespace uly {
 namespace {
 
 constexpr int BM = 128, BN = 128;
-constexpr int kThreads = 384;
-constexpr int kTmaWarp = 8, kMmaWarp = 9, kCvtWarp0 = 10;   // warps 10, 11 convert V
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 128 * 64 * 2;   // one [128 rows][64 elements] bf16 box
 
@@ -45,6 +44,7 @@ struct Layout {
 
 struct FwdArgs {
   __nv_bfloat16* o;
+  __nv_bfloat16* o_lo;   // optional: bf16(O - bf16(O)), for the backward's row terms
   float* lse;
   int S, hl, gl, group, n_mb;
   float scale_log2;
@@ -77,8 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* p_full = bars + 11;   // [2]
   uint64_t* o_done = bars + 13;   // [2]
   uint64_t* drain = bars + 15;
-  uint64_t* v16_ready = bars + 16;  // [2] V_j converted to fp16 in place
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 18);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -105,7 +104,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
-      mbar_init(&v16_ready[i], 64);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -158,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
-      constexpr uint32_t idesc_pv = idesc_f16(BM, D, false, true);   // fp16 P and V
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
       const bool stall = (a.flags & ULY_FLAG_INJECT_STALL) && blockIdx.x == 0;
       bool alive = mbar_wait(q_full, 0, wc);
       auto issue_s = [&](int t, int j) {
@@ -173,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto issue_pv = [&](int t, int j) -> bool {
         if (!mbar_wait(&p_full[t], j & 1, wc)) return false;
-        if (!mbar_wait(&v16_ready[j & 1], (j >> 1) & 1, wc)) return false;
+        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, wc)) return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + L::kV + (j & 1) * L::kTile);
 #pragma unroll
@@ -211,22 +209,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // All issued MMAs complete before TMEM can be freed.
       mma_commit(drain);
       mbar_drain(drain, 0, a.limit_ns);
-    }
-  } else if (warp >= kCvtWarp0) {
-    // V_j arrives in bf16; P.V runs on fp16 operands (P has 11 significand bits there),
-    // so these two warps convert every V tile in place once it has landed.
-    const int tid = (warp - kCvtWarp0) * 32 + lane;
-    for (int j = 0; j < n1; ++j) {
-      const int st = j & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&v_full[st], (j >> 1) & 1, wc))) break;
-      uint8_t* vt = smem + L::kV + st * L::kTile;
-#pragma unroll 4
-      for (int c = tid; c < L::kTile / 16; c += 64) {
-        uint4* p = reinterpret_cast<uint4*>(vt + c * 16);
-        *p = bf16x8_to_f16x8(*p);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(&v16_ready[st]);
     }
   } else {
     // Softmax warpgroups: t = query tile, one thread per row / TMEM lane.
@@ -281,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i]), sl2, -m_used));
           const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, -m_used));
           sum += p0 + p1;
-          pk[i] = pack_f16x2_sat(p0, p1);
+          pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(ts + 16 * c, pk);
       }
@@ -306,7 +288,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      __nv_bfloat16* orow = a.o + (((size_t)r * a.S + row_g) * a.hl + hh) * D;
+      const size_t orow_off = (((size_t)r * a.S + row_g) * a.hl + hh) * D;
+      __nv_bfloat16* orow = a.o + orow_off;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -320,6 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             v.z = pack_bf16x2(__uint_as_float(o[8 * j + 4]) * inv_l, __uint_as_float(o[8 * j + 5]) * inv_l);
             v.w = pack_bf16x2(__uint_as_float(o[8 * j + 6]) * inv_l, __uint_as_float(o[8 * j + 7]) * inv_l);
             *reinterpret_cast<uint4*>(orow + 32 * c + 8 * j) = v;
+            if (a.o_lo) {
+              // what the bf16 rounding of O dropped, itself in bf16
+              const uint32_t hw[4] = {v.x, v.y, v.z, v.w};
+              uint32_t lw[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 h = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[e]));
+                lw[e] = pack_bf16x2(__uint_as_float(o[8 * j + 2 * e]) * inv_l - h.x,
+                                    __uint_as_float(o[8 * j + 2 * e + 1]) * inv_l - h.y);
+              }
+              *reinterpret_cast<uint4*>(a.o_lo + orow_off + 32 * c + 8 * j) =
+                  make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
           }
         }
       }
@@ -339,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_fwd_d(const Plan& p, const void* q, const void* k, const void* v, void* o,
-                         float* lse, cudaStream_t st) {
+                         void* o_lo, float* lse, cudaStream_t st) {
   const int hl = p.H / p.P, gl = p.G / p.P;
   const char* err = nullptr;
   CUtensorMap tq, tk, tv;
@@ -353,6 +349,7 @@ cudaError_t launch_fwd_d(const Plan& p, const void* q, const void* k, const void
     return cudaErrorInvalidValue;
   FwdArgs a;
   a.o = static_cast<__nv_bfloat16*>(o);
+  a.o_lo = static_cast<__nv_bfloat16*>(o_lo);
   a.lse = lse;
   a.S = (int)p.S;
   a.hl = hl;
@@ -374,9 +371,9 @@ cudaError_t launch_fwd_d(const Plan& p, const void* q, const void* k, const void
 }  // namespace
 
 cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v, void* o,
-                            float* lse, cudaStream_t st) {
-  if (p.D == 64) return launch_fwd_d<64>(p, q, k, v, o, lse, st);
-  return launch_fwd_d<128>(p, q, k, v, o, lse, st);
+                            void* o_lo, float* lse, cudaStream_t st) {
+  if (p.D == 64) return launch_fwd_d<64>(p, q, k, v, o, o_lo, lse, st);
+  return launch_fwd_d<128>(p, q, k, v, o, o_lo, lse, st);
 }
 
 }  // namespace uly

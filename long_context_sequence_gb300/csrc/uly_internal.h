@@ -37,10 +37,11 @@ cudaError_t launch_permute_heads(const Plan& p, const void* in, int n_heads, voi
 cudaError_t launch_qkv_gemm(const Plan& p, const void* x, const void* w, void* out,
                             cudaStream_t st);
 cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v,
-                            void* o, float* lse, cudaStream_t st);
+                            void* o, void* o_lo, float* lse, cudaStream_t st);
 cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const void* v,
-                            const void* o, const float* lse, const void* d_o, void* dq,
-                            void* dk, void* dv, void* workspace, cudaStream_t st);
+                            const void* o, const void* o_lo, const float* lse,
+                            const void* d_o, void* dq, void* dk, void* dv, void* workspace,
+                            cudaStream_t st);
 
 // Workspace layout of the backward pass.
 size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off);

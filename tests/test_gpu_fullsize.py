@@ -58,12 +58,12 @@ def _bwd_check(S, P, H, G, D, std, n_rows, tail, tag):
     q, k, v = _gen(S, P, H, G, D, std)
     do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D))
     qg, kg, vg, dog = (dev_bf16(a) for a in (q, k, v, do))
-    o = empty_bf16((P, S, H // P, D))
+    o, o_lo = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, H // P, D))
     lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
-    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse)
+    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse, o_lo=o_lo)
     ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
     dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
-    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws)
+    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws, o_lo=o_lo)
     assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
     rows = synthetic.sample_rows(S, P, n_rows)
     dq_h, dk_h, dv_h = host_f64(dq), host_f64(dk), host_f64(dv)
@@ -90,17 +90,17 @@ def test_million_token_head_group_fwd_bwd():
     S, P, H, G, D = 1 << 20, 1, 4, 1, 128
     plan = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
     q, k, v = _gen(S, P, H, G, D, 1.0)
-    o = empty_bf16((P, S, H, D))
+    o, o_lo = empty_bf16((P, S, H, D)), empty_bf16((P, S, H, D))
     lse = torch.empty((P, H, S), dtype=torch.float32, device="cuda")
     qg, kg, vg = dev_bf16(q), dev_bf16(k), dev_bf16(v)
-    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse)
+    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse, o_lo=o_lo)
     assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
     rows = synthetic.sample_rows(S, 8, 256)
     _check_fwd_rows(q, k, v, o, lse, rows, P, H, G, "S=1M")
     do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H, D))
     ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
     dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
-    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dev_bf16(do), dq, dk, dv, ws)
+    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dev_bf16(do), dq, dk, dv, ws, o_lo=o_lo)
     assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
     rows = synthetic.sample_rows(S, 8, 64)
     qf, kf, vf, dof = (synthetic.bf16_to_f64(a[0]) for a in (q, k, v, do))

@@ -154,13 +154,13 @@ def test_attention_backward(S, P, H, G, D, std):
     q, k, v = _attn_inputs(S, P, H, G, D, std)
     do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D))
     qg, kg, vg, dog = (dev_bf16(a) for a in (q, k, v, do))
-    o = empty_bf16((P, S, H // P, D))
+    o, o_lo = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, H // P, D))
     lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
-    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse)
+    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse, o_lo=o_lo)
     ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
     ws.fill_(0xFF)   # contents on entry must not matter
     dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
-    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws)
+    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws, o_lo=o_lo)
     _ok(plan)
     qf, kf, vf, dof = (synthetic.bf16_to_f64(a) for a in (q, k, v, do))
     for r in range(P):
@@ -236,3 +236,31 @@ def test_misaligned_pointer_is_rejected_before_launch():
                            buf.data_ptr(), buf.data_ptr())
     assert ei.value.status == U.ULY_ERR_INVALID_ARG
     _ok(plan)
+
+
+def test_forward_rounding_residual_and_backward_without_it():
+    """o + o_lo reproduces the fp32 output to ~16 bits; the backward also runs without
+    o_lo (row terms from the bf16 o alone) and still meets the bound on the tiny shape."""
+    S, P, H, G, D = 1024, 4, 8, 8, 64
+    plan = _plan(S, P, H, G, D)
+    q, k, v = _attn_inputs(S, P, H, G, D, 0.45)
+    do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D))
+    qg, kg, vg, dog = (dev_bf16(a) for a in (q, k, v, do))
+    o, o_lo = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, H // P, D))
+    lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
+    U.ulysses_attn_fwd(plan, qg, kg, vg, o, lse, o_lo=o_lo)
+    ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+    dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
+    U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws)
+    _ok(plan)
+    qf, kf, vf, dof = (synthetic.bf16_to_f64(a) for a in (q, k, v, do))
+    ro, _ = O.ulysses_attention(qf, kf, vf)
+    hi, lo = host_f64(o), host_f64(o_lo)
+    assert np.all(np.abs(lo) <= np.abs(hi) * 2.0 ** -8 * 1.01 + 1e-30)   # about half a bf16 ulp
+    assert np.abs(hi + lo - ro).max() < np.abs(hi - ro).max()     # closer than o alone
+    assert np.abs(hi + lo - ro).max() < 2e-3
+    for r in range(P):
+        rdq, rdk, rdv = O.causal_attention_bwd(qf[r], kf[r], vf[r], dof[r])
+        assert_close(host_f64(dq)[r], rdq, "dq[rank %d] without o_lo" % r)
+        assert_close(host_f64(dk)[r], rdk, "dk[rank %d] without o_lo" % r)
+        assert_close(host_f64(dv)[r], rdv, "dv[rank %d] without o_lo" % r)
