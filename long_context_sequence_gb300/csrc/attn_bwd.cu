@@ -286,18 +286,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t sv[16], dp[16], pk[8], dk[8];
+        float lse2[16], dlt[16];
+        const float4* l4 = reinterpret_cast<const float4*>(rw + 32 * w + 16 * c);
+        const float4* d4 = reinterpret_cast<const float4*>(rw + 128 + 32 * w + 16 * c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 x = l4[e], y = d4[e];
+          lse2[4 * e] = x.x; lse2[4 * e + 1] = x.y; lse2[4 * e + 2] = x.z; lse2[4 * e + 3] = x.w;
+          dlt[4 * e] = y.x; dlt[4 * e + 1] = y.y; dlt[4 * e + 2] = y.z; dlt[4 * e + 3] = y.w;
+        }
         tmem_ld16(tbase + lane_off + 32 * w + 16 * c, sv);
         tmem_ld16(tbase + lane_off + 128 + 32 * w + 16 * c, dp);
+        if (need_mask) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int qg = q0 + 32 * w + 16 * c + e;
+            if (!(key_g <= qg && qg < a.S && key_g < a.S)) lse2[e] = INFINITY;  // p = 0
+          }
+        }
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {
           float pv[2], dv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int qc = 32 * w + 16 * c + 2 * i2 + e;
-            float p = ex2_approx(fmaf(__uint_as_float(sv[2 * i2 + e]), sl2, -rw[qc]));
-            if (need_mask && !(key_g <= q0 + qc && q0 + qc < a.S && key_g < a.S)) p = 0.f;
+            const int j = 2 * i2 + e;
+            const float p = ex2_approx(fmaf(__uint_as_float(sv[j]), sl2, -lse2[j]));
             pv[e] = p;
-            dv[e] = p * (__uint_as_float(dp[2 * i2 + e]) - rw[128 + qc]);
+            dv[e] = p * (__uint_as_float(dp[j]) - dlt[j]);
           }
           pk[i2] = pack_f16x2_sat(pv[0], pv[1]);
           dk[i2] = pack_f16x2_sat(dv[0], dv[1]);

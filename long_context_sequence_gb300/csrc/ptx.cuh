@@ -50,6 +50,20 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the instruction while
+// the phase is incomplete (fewer issue slots spent polling).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -77,8 +91,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    for (int i = 0; i < 8; ++i)
+      if (mbar_try_wait_sleep(bar, parity, 20000)) return true;
     if (*w.abort) return false;
     if (*reinterpret_cast<volatile int*>(w.status) != kOk) {   // another CTA gave up
       *w.abort = 1;
@@ -273,23 +287,20 @@ __device__ __forceinline__ float ex2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// fp16 pair, round to nearest even, clamped to the finite fp16 range.
+// fp16 pair (lo in the low half), round to nearest even, saturated to the finite range.
 __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-  lo = fminf(fmaxf(lo, -65504.f), 65504.f);
-  hi = fminf(fmaxf(hi, -65504.f), 65504.f);
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Two bf16 in one word -> two fp16 (a bf16 is the top half of its fp32 value).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
+  return pack_f16x2_sat(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 // 8 bf16 -> 8 fp16 (16 bytes in, 16 bytes out).
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
-  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&v);
-  uint4 o;
-  float2 f;
-  f = __bfloat1622float2(b[0]); o.x = pack_f16x2_sat(f.x, f.y);
-  f = __bfloat1622float2(b[1]); o.y = pack_f16x2_sat(f.x, f.y);
-  f = __bfloat1622float2(b[2]); o.z = pack_f16x2_sat(f.x, f.y);
-  f = __bfloat1622float2(b[3]); o.w = pack_f16x2_sat(f.x, f.y);
-  return o;
+  return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
+                    bf16x2_to_f16x2(v.w));
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
