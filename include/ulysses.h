@@ -141,6 +141,22 @@ uly_status ulysses_attn_bwd(uly_plan plan, const void *q, const void *k, const v
                             const void *d_o, void *dq, void *dk, void *dv, void *workspace,
                             void *stream);
 
+/* ulysses_attn_bwd without a caller-provided workspace.  The pages have no counterpart:
+ * this serves callers that cannot allocate device memory at call time -- a program that
+ * has handed all of HBM to its own pool or caching allocator, a latency-critical path
+ * that must not pay cudaMalloc's implicit synchronisation, a plain C caller without a
+ * device allocator.  Same arguments and results as ulysses_attn_bwd (minus workspace).
+ * The scratch is a fixed 64 MiB array inside the library's device memory (held by every
+ * GPU that loads the library until the process exits); plans whose backward needs more
+ * (ulysses_workspace_bytes) get ULY_ERR_UNSUPPORTED and nothing is launched.  The first
+ * call on each device looks the array's address up (make it before any stream capture);
+ * no call allocates.  All calls share the array: calls that may overlap on the GPU race,
+ * so order them (e.g. one stream).  The plan's device must be the current device. */
+uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void *q, const void *k,
+                                    const void *v, const void *o, const void *o_lo,
+                                    const float *lse, const void *d_o, void *dq, void *dk,
+                                    void *dv, void *stream);
+
 /* head->seq all-to-all, the inverse of seq->head ("another all-to-all operation reverses
  * the redistribution", Hugging Face post para 5): x_head [P][S][n_heads/P][D] ->
  * x_seq [P][S/P][n_heads][D].  n_heads = H for o and dq, G for dk and dv. */

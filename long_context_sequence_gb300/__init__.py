@@ -21,7 +21,8 @@ _STATUS_NAMES = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED"
 
 EXPORTED = ("ulysses_plan", "ulysses_plan_destroy", "ulysses_workspace_bytes",
             "ulysses_qkv_proj", "ulysses_seq_to_head", "ulysses_seq_to_head_heads",
-            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_head_to_seq",
+            "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc",
+            "ulysses_head_to_seq",
             "ulysses_sync_status", "ulysses_bytes_moved", "ulysses_a2a_volume",
             "ulysses_last_error")
 
@@ -72,6 +73,7 @@ def load_library(path: str = LIB_PATH):
         "ulysses_seq_to_head_heads": ([vp, vp, i32, vp, vp], i32),
         "ulysses_attn_fwd": ([vp] * 8, i32),
         "ulysses_attn_bwd": ([vp] * 13, i32),
+        "ulysses_attn_bwd_noalloc": ([vp] * 12, i32),
         "ulysses_head_to_seq": ([vp, vp, i32, vp, vp], i32),
         "ulysses_sync_status": ([vp, vp], i32),
         "ulysses_bytes_moved": ([vp], u64),
@@ -185,6 +187,14 @@ def ulysses_attn_bwd(plan, q, k, v, o, lse, d_o, dq, dk, dv, workspace, stream=N
                                            _ptr(o_lo), _ptr(lse), _ptr(d_o), _ptr(dq),
                                            _ptr(dk), _ptr(dv), _ptr(workspace),
                                            _stream(stream)))
+
+
+def ulysses_attn_bwd_noalloc(plan, q, k, v, o, lse, d_o, dq, dk, dv, stream=None, o_lo=None):
+    """The backward with the library's fixed device scratch instead of a workspace."""
+    _check(load_library().ulysses_attn_bwd_noalloc(plan.handle, _ptr(q), _ptr(k), _ptr(v),
+                                                   _ptr(o), _ptr(o_lo), _ptr(lse), _ptr(d_o),
+                                                   _ptr(dq), _ptr(dk), _ptr(dv),
+                                                   _stream(stream)))
 
 
 def ulysses_head_to_seq(plan, x_head, n_heads, x_seq, stream=None):

@@ -103,15 +103,19 @@ bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims_in[
   return true;
 }
 
+uly_status set_error(uly_status s, const char* msg) {
+  if (s == ULY_OK) {
+    g_err[0] = 0;
+    return s;
+  }
+  return fail(s, "%s", msg);
+}
+
 }  // namespace uly
 
 using uly::Plan;
 using uly::aligned16;
 using uly::fail;
-
-struct uly_plan_s {
-  Plan p;
-};
 
 namespace {
 

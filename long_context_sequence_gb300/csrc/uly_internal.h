@@ -29,6 +29,9 @@ struct Plan {
   std::atomic<uint64_t> bytes_moved{0};
 };
 
+// Records msg as the thread's last error (ULY_OK clears it) and returns s.
+uly_status set_error(uly_status s, const char* msg);
+
 // Launchers: each validates nothing (api.cu did) and returns the launch error.
 cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool rope, void* q,
                                void* k, void* v, cudaStream_t st);
@@ -60,3 +63,8 @@ bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4],
 int num_sms(int device);
 
 }  // namespace uly
+
+// The opaque handle of the C ABI.
+struct uly_plan_s {
+  uly::Plan p;
+};
