@@ -93,8 +93,9 @@ uly_status ulysses_plan(const uly_config *cfg, uly_plan *out);
 /* Frees the plan's buffers.  NULL is allowed.  Synchronises the device first. */
 uly_status ulysses_plan_destroy(uly_plan plan);
 
-/* Bytes of scratch that ulysses_attn_bwd needs: an fp32 dQ accumulator [P][S][H/P][D]
- * followed by the fp32 row terms Delta [P][H/P][S], each part 256-byte aligned. */
+/* Bytes of scratch that ulysses_attn_bwd needs: an fp32 dQ accumulator [P][S][H/P][D],
+ * the fp32 row terms Delta [P][H/P][S] and fp16 copies of q, d_o, k and v, each part
+ * 256-byte aligned. */
 size_t ulysses_workspace_bytes(uly_plan plan);
 
 /* Local QKV projection of every shard ("each rank computes its local QKV projection",

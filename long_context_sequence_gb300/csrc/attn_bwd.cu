@@ -9,7 +9,8 @@
 //
 // Three kernels:
 //   bwd_pre   D_i = dO_i . (o_i + o_lo_i) in fp32 (o_lo: the forward's optional bf16 rounding
-//             residual of O) and zeroing of the fp32 dQ accumulator;
+//             residual of O), zeroing of the fp32 dQ accumulator, and fp16 copies of Q,
+//             dO (and, in to_f16_kernel, of K, V) for the tensor-core operands;
 //   bwd_main  one CTA per (rank, KV head, 128-key block), looping over the group's query
 //             heads and the causally visible 128-row query tiles ("items"):
 //               MMA1   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 128 rows)
@@ -19,11 +20,12 @@
 //               MMA2   dQ^T = K^T dS^T (M = d, TMEM over S^T), dV += P^T dO, dK += dS^T Q
 //               the same 16 warps, thread = d: dQ^T -> fp32 reductions into the workspace
 //                      accumulator (one 128-byte run per warp and row);
-//             while MMA2 runs they also convert the next item's Q and dO tiles.
 //   bwd_dq    fp32 dQ accumulator -> bf16.
-// Every MMA runs on fp16 operands: K, V (once per CTA) and each Q, dO tile are converted in
-// place from bf16 (exact for magnitudes in [2^-14, 65504]; clamped outside), and P, dS
-// keep 11 significand bits, which the long dK/dQ sums need.
+// Every MMA runs on fp16 operands: the fp16 copies of Q, K, V, dO made by the pre-pass
+// (exact for magnitudes in [2^-14, 65504]; saturated outside), and P, dS keep 11
+// significand bits, which the long dK/dQ sums need.  P is formed as scale * P (the scale
+// folded into the exponent), so dS, dQ^T and dK come out scaled and dV is divided by the
+// scale once at the end.
 // TMEM (512 columns): S^T [0,128) -> dQ^T (rows 0-63 at [0,64), 64-127 at [64,128));
 // dP^T [128,256) -> P^T of warpgroup w at [128+32w, 128+32w+16); dV [256,256+D),
 // dK [256+D, 256+2D).
@@ -64,22 +66,13 @@ struct BwdArgs {
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int S, hl, gl, group, nkb;
-  float scale, scale_log2;
+  float scale, scale_log2, log2_scale;
   int* status;
   uint64_t limit_ns;
 };
 
 __device__ __forceinline__ void red_add(float* addr, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
-// bf16 -> fp16 in place over [base, base + bytes), by `n` threads with index t.
-__device__ __forceinline__ void convert_tile(uint8_t* base, int bytes, int t, int n) {
-#pragma unroll 4
-  for (int c = t; c < bytes / 16; c += n) {
-    uint4* p = reinterpret_cast<uint4*>(base + c * 16);
-    *p = bf16x8_to_f16x8(*p);
-  }
 }
 
 template <int D>
@@ -96,17 +89,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* rows = reinterpret_cast<float*>(smem + L::kRow);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* kv_full = bars + 0;
-  uint64_t* kv16 = bars + 1;
-  uint64_t* qd_full = bars + 2;              // [NST]
-  uint64_t* qd_empty = bars + 2 + NST;       // [NST]
-  uint64_t* conv = bars + 2 + 2 * NST;
-  uint64_t* s_full = conv + 1;
-  uint64_t* p_full = conv + 2;
-  uint64_t* dq_full = conv + 3;
-  uint64_t* dq_free = conv + 4;
-  uint64_t* acc_done = conv + 5;
-  uint64_t* drain = conv + 6;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(conv + 7);
+  uint64_t* qd_full = bars + 1;              // [NST]
+  uint64_t* qd_empty = bars + 1 + NST;       // [NST]
+  uint64_t* s_full = bars + 1 + 2 * NST;
+  uint64_t* p_full = s_full + 1;
+  uint64_t* dq_full = s_full + 2;
+  uint64_t* dq_free = s_full + 3;
+  uint64_t* acc_done = s_full + 4;
+  uint64_t* drain = s_full + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 6);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -120,12 +111,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(kv16, kCompute);
     for (int i = 0; i < NST; ++i) {
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
-    mbar_init(conv, kCompute);
     mbar_init(s_full, 1);
     mbar_init(p_full, kCompute);
     mbar_init(dq_full, 1);
@@ -152,11 +141,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_do);
-      mbar_arrive_expect_tx(kv_full, 2 * L::kKV);
-      for (int b = 0; b < D / 64; ++b) {
+      // K always as two 64-column atoms: for D = 64 the second box lies past the last
+      // column and TMA fills it with zeros (the zero rows of K^T padded to M = 128).
+      mbar_arrive_expect_tx(kv_full, 2 * kBox + L::kKV);
+      for (int b = 0; b < 2; ++b)
         tma_load_4d(smem + L::kK + b * kBox, &tm_k, kv_full, 64 * b, gg, nb * BN, r);
+      for (int b = 0; b < D / 64; ++b)
         tma_load_4d(smem + L::kV + b * kBox, &tm_v, kv_full, 64 * b, gg, nb * BN, r);
-      }
     }
     int issued = 0;
     for (int it = 0; it < n_items; ++it) {
@@ -171,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qc = lane + 32 * e;
         const int qg = i * BM + qc;
         const size_t idx = ((size_t)r * a.hl + hh) * a.S + qg;
-        rw[qc] = qg < a.S ? a.lse[idx] * 1.4426950408889634f : INFINITY;
+        rw[qc] = qg < a.S ? a.lse[idx] * 1.4426950408889634f - a.log2_scale : INFINITY;
         rw[128 + qc] = qg < a.S ? a.delta[idx] : 0.f;
       }
       __syncwarp();
@@ -198,12 +189,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_kv = idesc_f16(BN, D, false, true);    // dV, dK
       const uint32_t sK = smem_u32(smem + L::kK), sV = smem_u32(smem + L::kV);
       const uint32_t sDS = smem_u32(smem + L::kDS);
-      bool alive = mbar_wait(kv16, 0, wc);
+      bool alive = mbar_wait(kv_full, 0, wc);
       for (int it = 0; alive && it < n_items; ++it) {
         const int st = it % NST;
         const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kKV);
         const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kKV);
-        if (!mbar_wait(conv, it & 1, wc)) break;
+        if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) break;
         if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
@@ -253,26 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = a.scale_log2;
     uint8_t* ds_row = smem + L::kDS + (w / 2) * kBox + row * 128;
-    bool ok = __all_sync(0xffffffffu, mbar_wait(kv_full, 0, wc));
-    if (ok) {
-      // K, V to fp16 in place; for D = 64 the second K atom (read by dQ^T) is zero.
-      convert_tile(smem + L::kK, L::kKV, threadIdx.x, kCompute);
-      convert_tile(smem + L::kV, L::kKV, threadIdx.x, kCompute);
-      if (D == 64)
-        for (int c = threadIdx.x; c < kBox / 16; c += kCompute)
-          *reinterpret_cast<uint4*>(smem + L::kK + kBox + c * 16) = make_uint4(0, 0, 0, 0);
-      fence_proxy_async_smem();
-    }
-    mbar_arrive(kv16);
-    if (ok && n_items > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&qd_full[0], 0, wc));
-      if (ok) {
-        convert_tile(smem + L::kQ, L::kKV, threadIdx.x, kCompute);
-        convert_tile(smem + L::kDO, L::kKV, threadIdx.x, kCompute);
-        fence_proxy_async_smem();
-        mbar_arrive(conv);
-      }
-    }
+    bool ok = true;
     for (int it = 0; ok && it < n_items; ++it) {
       const int st = it % NST;
       const int i = nb + it / a.group;
@@ -335,16 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(p_full);
-      // While MMA2 runs: convert the next item's Q and dO, then read dQ^T out.
-      if (it + 1 < n_items) {
-        const int st1 = (it + 1) % NST;
-        ok = __all_sync(0xffffffffu, mbar_wait(&qd_full[st1], ((it + 1) / NST) & 1, wc));
-        if (!ok) break;
-        convert_tile(smem + L::kQ + st1 * L::kKV, L::kKV, threadIdx.x, kCompute);
-        convert_tile(smem + L::kDO + st1 * L::kKV, L::kKV, threadIdx.x, kCompute);
-        fence_proxy_async_smem();
-        mbar_arrive(conv);
-      }
+      // While dV and dK run: read dQ^T out (already scaled, see the row terms).
       ok = __all_sync(0xffffffffu, mbar_wait(dq_full, it & 1, wc));
       if (!ok) break;
       tc_fence_after();
@@ -355,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const size_t rs = (size_t)a.hl * D;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if (q0 + 32 * w + j < a.S) red_add(base + j * rs, __uint_as_float(v[j]) * a.scale);
+          if (q0 + 32 * w + j < a.S) red_add(base + j * rs, __uint_as_float(v[j]));
       }
       tc_fence_before();
       mbar_arrive(dq_free);
@@ -367,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int which = w / 2;            // 0: dV, 1: dK
       const int half = w % 2;             // columns [32*half*(D/64), ...)
       __nv_bfloat16* dst = (which ? a.dk : a.dv) + (((size_t)r * a.S + key_g) * a.gl + gg) * D;
-      const float mul = which ? a.scale : 1.f;
+      const float mul = which ? 1.f : 1.f / a.scale;   // the dV sums carry the scale
 #pragma unroll 1
       for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t v[32];
@@ -403,8 +366,11 @@ template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ o_lo,
                                                       const __nv_bfloat16* __restrict__ d_o,
+                                                      const __nv_bfloat16* __restrict__ q,
                                                       float* __restrict__ delta,
-                                                      float* __restrict__ dq_acc, int64_t rows,
+                                                      float* __restrict__ dq_acc,
+                                                      uint4* __restrict__ q16,
+                                                      uint4* __restrict__ do16, int64_t rows,
                                                       int64_t S, int hl) {
   constexpr int TPR = D / 8;
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -429,6 +395,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     float4* zq = reinterpret_cast<float4*>(dq_acc + rowid * D + part * 8);
     zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    // fp16 copies of dO and Q for the main kernel's tensor-core operands
+    do16[(rowid * D + part * 8) / 8] = bf16x8_to_f16x8(b);
+    q16[(rowid * D + part * 8) / 8] =
+        bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(q + rowid * D + part * 8));
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -438,6 +408,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const int64_t r = rs / S, s = rs - r * S;
     delta[(r * hl + hh) * S + s] = acc;
   }
+}
+
+// bf16 -> fp16 copy, 8 elements per thread (K and V for the main kernel).
+__global__ void __launch_bounds__(256) to_f16_kernel(const uint4* __restrict__ src,
+                                                     uint4* __restrict__ dst, int64_t n8) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = bf16x8_to_f16x8(src[i]);
 }
 
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
@@ -460,19 +438,32 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
                          const void* o, const void* o_lo, const float* lse, const void* d_o,
                          void* dq, void* dk, void* dv, void* workspace, cudaStream_t st) {
   const int hl = p.H / p.P, gl = p.G / p.P;
-  size_t acc_off = 0, delta_off = 0;
-  bwd_workspace_bytes(p, &acc_off, &delta_off);
-  float* dq_acc = reinterpret_cast<float*>(static_cast<char*>(workspace) + acc_off);
-  float* delta = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_off);
+  const BwdWorkspace ws = bwd_workspace_layout(p);
+  char* wsb = static_cast<char*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(wsb + ws.dq_acc);
+  float* delta = reinterpret_cast<float*>(wsb + ws.delta);
+  void* q16 = wsb + ws.q16;
+  void* do16 = wsb + ws.do16;
+  void* k16 = wsb + ws.k16;
+  void* v16 = wsb + ws.v16;
   const int64_t rows = (int64_t)p.P * p.S * hl;
   {
     const int64_t threads = rows * (D / 8);
     const int64_t blocks = (threads + 255) / 256;
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(o_lo),
-        static_cast<const __nv_bfloat16*>(d_o), delta,
-        dq_acc, rows, p.S, hl);
+        static_cast<const __nv_bfloat16*>(d_o), static_cast<const __nv_bfloat16*>(q), delta,
+        dq_acc, static_cast<uint4*>(q16), static_cast<uint4*>(do16), rows, p.S, hl);
     cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int64_t n8 = (int64_t)p.P * p.S * gl * D / 8;
+    const int64_t cap = (int64_t)num_sms(p.device) * 16;
+    const int64_t b8 = std::min<int64_t>((n8 + 255) / 256, cap);
+    to_f16_kernel<<<(unsigned)b8, 256, 0, st>>>(static_cast<const uint4*>(k),
+                                                 static_cast<uint4*>(k16), n8);
+    to_f16_kernel<<<(unsigned)b8, 256, 0, st>>>(static_cast<const uint4*>(v),
+                                                 static_cast<uint4*>(v16), n8);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   const char* err = nullptr;
@@ -481,10 +472,11 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)hl * D * 2, (uint64_t)p.S * hl * D * 2};
   const uint64_t dk4[4] = {(uint64_t)D, (uint64_t)gl, (uint64_t)p.S, (uint64_t)p.P};
   const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)gl * D * 2, (uint64_t)p.S * gl * D * 2};
-  if (!make_tmap_4d_bf16(&tq, q, dq4, sq, 64, BM, &err) ||
-      !make_tmap_4d_bf16(&tdo, d_o, dq4, sq, 64, BM, &err) ||
-      !make_tmap_4d_bf16(&tk, k, dk4, sk, 64, BN, &err) ||
-      !make_tmap_4d_bf16(&tv, v, dk4, sk, 64, BN, &err))
+  // the maps read the fp16 copies (TMA moves 16-bit elements either way)
+  if (!make_tmap_4d_bf16(&tq, q16, dq4, sq, 64, BM, &err) ||
+      !make_tmap_4d_bf16(&tdo, do16, dq4, sq, 64, BM, &err) ||
+      !make_tmap_4d_bf16(&tk, k16, dk4, sk, 64, BN, &err) ||
+      !make_tmap_4d_bf16(&tv, v16, dk4, sk, 64, BN, &err))
     return cudaErrorInvalidValue;
   BwdArgs a;
   a.lse = lse;
@@ -499,6 +491,7 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   a.nkb = (int)((p.S + BN - 1) / BN);
   a.scale = p.scale;
   a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.log2_scale = log2f(p.scale);
   a.status = p.status;
   a.limit_ns = p.limit_ns;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
@@ -518,14 +511,26 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
 
 }  // namespace
 
+BwdWorkspace bwd_workspace_layout(const Plan& p) {
+  const size_t hl = p.H / p.P, gl = p.G / p.P, S = (size_t)p.S, P = p.P, D = p.D;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  BwdWorkspace w;
+  size_t off = 0;
+  w.dq_acc = off; off += al(P * S * hl * D * sizeof(float));
+  w.delta = off;  off += al(P * hl * S * sizeof(float));
+  w.q16 = off;    off += al(P * S * hl * D * 2);
+  w.do16 = off;   off += al(P * S * hl * D * 2);
+  w.k16 = off;    off += al(P * S * gl * D * 2);
+  w.v16 = off;    off += al(P * S * gl * D * 2);
+  w.total = off;
+  return w;
+}
+
 size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off) {
-  const int hl = p.H / p.P;
-  const size_t acc = (size_t)p.P * p.S * hl * p.D * sizeof(float);
-  const size_t acc_al = (acc + 255) & ~size_t(255);
-  const size_t dl = (size_t)p.P * hl * p.S * sizeof(float);
-  if (dq_acc_off) *dq_acc_off = 0;
-  if (delta_off) *delta_off = acc_al;
-  return acc_al + ((dl + 255) & ~size_t(255));
+  const BwdWorkspace w = bwd_workspace_layout(p);
+  if (dq_acc_off) *dq_acc_off = w.dq_acc;
+  if (delta_off) *delta_off = w.delta;
+  return w.total;
 }
 
 cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const void* v,

@@ -46,7 +46,12 @@ cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const v
                             const void* d_o, void* dq, void* dk, void* dv, void* workspace,
                             cudaStream_t st);
 
-// Workspace layout of the backward pass.
+// Workspace layout of the backward pass (byte offsets, each 256-aligned): fp32 dQ
+// accumulator, fp32 row terms, fp16 copies of q, dO, k, v.
+struct BwdWorkspace {
+  size_t dq_acc, delta, q16, do16, k16, v16, total;
+};
+BwdWorkspace bwd_workspace_layout(const Plan& p);
 size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off);
 
 // Tensor maps (TMA descriptors), built on the host through the driver entry point.
