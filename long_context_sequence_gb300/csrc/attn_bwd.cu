@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = s_full + 9;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 10);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int per_rank = a.gl * a.nkb;
@@ -128,9 +129,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kRegionThreads);
+      mbar_init(&p_full[i], 1);
       mbar_init(&dq_full[i], 1);
-      mbar_init(&dq_free[i], kRegionThreads);
+      mbar_init(&dq_free[i], 1);
     }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
@@ -274,13 +275,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t treg = tbase + lane_off + 128 * X;
     const float sl2 = a.scale_log2;
     uint8_t* ds_row = smem + L::kDS + X * kBox + row * 128;
+    // The region's first warp waits on the mbarrier; the other seven sleep in a named
+    // barrier (no issue slots) and read the outcome it left, so they all decide alike.
+    const bool leader = (warp % 8) == 0;
+    int n_waits = 0;
+    auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      volatile int* slot = decision + 2 * X + (n_waits & 1);
+      if (leader) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
+        if (lane == 0) *slot = got ? 1 : 0;
+      }
+      named_bar_sync(1 + X, kRegionThreads);
+      ++n_waits;
+      return *slot != 0;
+    };
+    // All threads of the region have finished (their own TMEM/smem writes fenced); one
+    // thread then arrives for the whole region.
+    auto group_arrive = [&](uint64_t* bar) {
+      named_bar_sync(1 + X, kRegionThreads);
+      if (leader && lane == 0) mbar_arrive(bar);
+    };
     bool ok = true;
     for (int it = X; ok && it < n_items; it += 2) {
       const int u = it >> 1, st = it % NST;
       int q0, hh;
       item_coords(it, nb, gg, a.group, q0, hh);
       const float* rw = rows + st * 128;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[X], u & 1, wc));
+      ok = group_wait(&s_full[X], u & 1);
       if (!ok) break;
       tc_fence_after();
       const bool need_mask = (q0 < nb * BN + BN) || (q0 + BMI > a.S) || (nb * BN + BN > a.S);
@@ -335,9 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[X]);
+      group_arrive(&p_full[X]);
       // dQ^T of this item (already scaled) -> the workspace accumulator
-      ok = __all_sync(0xffffffffu, mbar_wait(&dq_full[X], u & 1, wc));
+      ok = group_wait(&dq_full[X], u & 1);
       if (!ok) break;
       tc_fence_after();
       if (quarter * 32 < D) {   // warp-uniform: lanes are d = 32*quarter + lane
@@ -350,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q0 + 32 * w2 + j < a.S) red_add(base + j * rs, __uint_as_float(v[j]));
       }
       tc_fence_before();
-      mbar_arrive(&dq_free[X]);
+      group_arrive(&dq_free[X]);
     }
     // dV (warps 0-7) and dK (8-15) of this key block, once every MMA has finished.
     if (ok && n_items > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, wc));
