@@ -336,9 +336,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = group_wait(dq_full, it & 1);
       if (!ok) break;
       tc_fence_after();
-      if (quarter * 32 < D) {   // warp-uniform: lanes are d = 32*quarter + lane
-        uint32_t v[32];
-        tmem_ld32(tbase + lane_off + 32 * w, v);
+      // dQ^T to registers, hand the TMEM columns back at once (the next item's MMA1
+      // writes them), then issue the reductions from registers while MMA1 runs.
+      uint32_t v[32];
+      const bool has_d = quarter * 32 < D;   // warp-uniform: lanes are d = 32*quarter + lane
+      if (has_d) tmem_ld32(tbase + lane_off + 32 * w, v);
+      tc_fence_before();
+      group_arrive(dq_free);
+      if (has_d) {
         float* ptr = a.dq_acc + (((size_t)r * a.S + q0 + 32 * w) * a.hl + hh) * D + row;
         const int rs = a.hl * D;
         if (q0 + 32 * w + 32 <= a.S) {
@@ -350,8 +355,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q0 + 32 * w + j < a.S) red_add(ptr + j * rs, __uint_as_float(v[j]));
         }
       }
-      tc_fence_before();
-      group_arrive(dq_free);
     }
     // dV (warpgroups 0, 1) and dK (2, 3) of this key block.
     if (ok && n_items > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, wc));
