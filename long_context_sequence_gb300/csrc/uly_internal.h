@@ -65,6 +65,11 @@ bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
                        const char** err);
 
+// 4-D fp32 map without swizzle (box {box0, 1, box2, 1}); used as a TMA reduce target.
+bool make_tmap_4d_f32(CUtensorMap* m, const void* base, const uint64_t dims[4],
+                      const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
+                      const char** err);
+
 int num_sms(int device);
 
 }  // namespace uly
