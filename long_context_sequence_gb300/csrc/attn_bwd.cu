@@ -18,9 +18,8 @@
 //                      P^T = exp2(S^T scale log2e - lse log2e) -> TMEM (fp16),
 //                      dS = P (dP - D) -> smem (fp16, 128-byte swizzle)
 //               MMA2   dQ^T = K^T dS^T (M = d, TMEM over S^T), dV += P^T dO, dK += dS^T Q
-//               the same 16 warps, thread = d: dQ^T -> registers -> the item's Q/dO stage
-//                      (32 x 32 fp32 block per warp) -> TMA tensor reduce-add into the
-//                      workspace's fp32 accumulator (one bulk operation per warp);
+//               the same 16 warps, thread = d: dQ^T -> fp32 reductions into the workspace
+//                      accumulator (one 128-byte run per warp and row);
 //   bwd_dq    fp32 dQ accumulator -> bf16.
 // Every MMA runs on fp16 operands: the fp16 copies of Q, K, V, dO made by the pre-pass
 // (exact for magnitudes in [2^-14, 65504]; saturated outside), and P, dS keep 11
@@ -72,11 +71,38 @@ struct BwdArgs {
   uint64_t limit_ns;
 };
 
+__device__ __forceinline__ void red_add(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void red_add4(float* addr, float x, float y, float z, float w) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(x), "f"(y),
+               "f"(z), "f"(w)
+               : "memory");
+}
+
+// 4 x 4 transpose inside each group of 4 lanes: lane b holds x[k] = M[row b][col k]; on
+// return it holds x[k] = M[row k][col b] (two butterfly rounds of shuffles).
+__device__ __forceinline__ void quad_transpose(float (&x)[4], int lane) {
+  const bool odd = lane & 1, hi = lane & 2;
+  float s0 = odd ? x[0] : x[1], s1 = odd ? x[2] : x[3];
+  float r0 = __shfl_xor_sync(0xffffffffu, s0, 1), r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+  float y0 = odd ? r0 : x[0], y1 = odd ? x[1] : r0;
+  float y2 = odd ? r1 : x[2], y3 = odd ? x[3] : r1;
+  s0 = hi ? y0 : y2;
+  s1 = hi ? y1 : y3;
+  r0 = __shfl_xor_sync(0xffffffffu, s0, 2);
+  r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
+  x[0] = hi ? r0 : y0;
+  x[1] = hi ? r1 : y1;
+  x[2] = hi ? y2 : r0;
+  x[3] = hi ? y3 : r1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const __grid_constant__ CUtensorMap tm_dq, const BwdArgs a) {
+                    const BwdArgs a) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {   // the swizzled tiles need 1024-byte alignment
@@ -215,6 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(s_full);
         if (!mbar_wait(p_full, it & 1, wc)) break;
         tc_fence_after();
+        // dQ^T first: its read-out overlaps the dV and dK MMAs.
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss(tbase + 64 * h, dK_mn + ((kk * 2048) >> 4),
+                   dDS_mn + ((h * kBox + kk * 2048) >> 4), id_q, kk > 0 ? 1u : 0u);
+        mma_commit(dq_full);
 #pragma unroll
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_ts(tbase + 256, tbase + 128 + 32 * (kk / 2) + 8 * (kk % 2),
@@ -223,15 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BM / 16; ++kk)
           mma_ss(tbase + 256 + D, dDS_k + (((kk / 4) * kBox + (kk % 4) * 32) >> 4),
                  dQ_mn + ((kk * 2048) >> 4), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tbase + 64 * h, dK_mn + ((kk * 2048) >> 4),
-                   dDS_mn + ((h * kBox + kk * 2048) >> 4), id_q, kk > 0 ? 1u : 0u);
-        // every MMA of the item is done once this fires: dQ^T may be read and the Q/dO
-        // stage reused as the staging buffer of the dQ reduction
-        mma_commit(dq_full);
+        mma_commit(&qd_empty[st]);
       }
       if (alive) mma_commit(acc_done);
       mma_commit(drain);
@@ -334,32 +360,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       // dQ^T to registers, hand the TMEM columns back at once (the next item's MMA1
-      // writes them); then each warp stages its 32 (rows) x 32 (d) block in the item's
-      // Q/dO stage (free now) and one lane has TMA add it into the fp32 accumulator.
+      // writes them), then issue the reductions from registers while MMA1 runs.
       uint32_t v[32];
       const bool has_d = quarter * 32 < D;   // warp-uniform: lanes are d = 32*quarter + lane
       if (has_d) tmem_ld32(tbase + lane_off + 32 * w, v);
       tc_fence_before();
       group_arrive(dq_free);
       if (has_d) {
-        constexpr int kHalf = 2 * (D / 32);          // 4 KB blocks that fit in one tile
-        const int b = w * (D / 32) + quarter;
-        float* blk = reinterpret_cast<float*>(
-            smem + (b < kHalf ? L::kQ : L::kDO) + st * L::kKV + (b % kHalf) * 4096);
+        // After a 4 x 4 transpose within each group of 4 lanes, lane 4g + b holds d values
+        // 32*quarter + 4g .. +3 of query row 4c + b: one 16-byte vector reduction each.
+        const int g4 = lane >> 2, b4 = lane & 3;
+        float* ptr = a.dq_acc + (((size_t)r * a.S + q0 + 32 * w + b4) * a.hl + hh) * D +
+                     32 * quarter + 4 * g4;
+        const int rs = a.hl * D;
+        const bool full = q0 + 32 * w + 32 <= a.S;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) blk[j * 32 + lane] = __uint_as_float(v[j]);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_reduce_add_4d(&tm_dq, blk, 32 * quarter, hh, q0 + 32 * w, r);
-          bulk_commit_group();
-          bulk_wait_read_all();
+        for (int c = 0; c < 8; ++c) {
+          float x[4] = {__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                        __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])};
+          quad_transpose(x, lane);
+          if (full || q0 + 32 * w + 4 * c + b4 < a.S)
+            red_add4(ptr + 4 * c * rs, x[0], x[1], x[2], x[3]);
         }
-        __syncwarp();
       }
-      group_arrive(&qd_empty[st]);
     }
-    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     // dV (warpgroups 0, 1) and dK (2, 3) of this key block.
     if (ok && n_items > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, wc));
     if (ok && n_items > 0) {
@@ -515,9 +539,6 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
       !make_tmap_4d_bf16(&tk, k16, dk4, sk, 64, BN, &err) ||
       !make_tmap_4d_bf16(&tv, v16, dk4, sk, 64, BN, &err))
     return cudaErrorInvalidValue;
-  CUtensorMap tdq;
-  const uint64_t dqs[3] = {(uint64_t)D * 4, (uint64_t)hl * D * 4, (uint64_t)p.S * hl * D * 4};
-  if (!make_tmap_4d_f32(&tdq, dq_acc, dq4, dqs, 32, 32, &err)) return cudaErrorInvalidValue;
   BwdArgs a;
   a.lse = lse;
   a.delta = delta;
@@ -539,8 +560,7 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
                                        BwdLayout<D>::kBytes);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.P * gl * a.nkb;
-  attn_bwd_kernel<D><<<(unsigned)blocks, kThreads, BwdLayout<D>::kBytes, st>>>(tq, tk, tv, tdo,
-                                                                             tdq, a);
+  attn_bwd_kernel<D><<<(unsigned)blocks, kThreads, BwdLayout<D>::kBytes, st>>>(tq, tk, tv, tdo, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * D / 8;
