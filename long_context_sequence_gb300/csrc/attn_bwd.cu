@@ -11,14 +11,16 @@
 //   bwd_pre   D_i = dO_i . (o_i + o_lo_i) in fp32 (o_lo: the forward's optional bf16 rounding
 //             residual of O), zeroing of the fp32 dQ accumulator, and fp16 copies of Q,
 //             dO (and, in to_f16_kernel, of K, V) for the tensor-core operands;
-//   bwd_main  one CTA per (rank, KV head, 128-key block), looping over the group's query
-//             heads and the causally visible 128-row query tiles ("items"):
-//               MMA1   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 128 rows)
-//               16 warps, thread = key row, warpgroup w = query columns [32w, 32w+32):
-//                      P^T = exp2(S^T scale log2e - lse log2e) -> TMEM (fp16),
+//   bwd_main  one CTA per (rank, KV head, 128-key block).  Work items are (64-row query
+//             tile, query head of the group) pairs from the diagonal on.  Items alternate
+//             between two TMEM regions so that one item's tensor work overlaps the other's
+//             element-wise work; the MMA warp issues MMA2(it) then MMA1(it+2):
+//               MMA1   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 64 rows)
+//               8 warps per region, thread = key row, warpgroup = 32 query columns:
+//                      P^T = scale*exp(S^T scale - lse) -> TMEM (fp16, over dP^T),
 //                      dS = P (dP - D) -> smem (fp16, 128-byte swizzle)
-//               MMA2   dQ^T = K^T dS^T (M = d, TMEM over S^T), dV += P^T dO, dK += dS^T Q
-//               the same 16 warps, thread = d: dQ^T -> fp32 reductions into the workspace
+//               MMA2   dQ^T = K^T dS^T (M = d, over S^T), dV += P^T dO, dK += dS^T Q
+//               the same warps, thread = d: dQ^T -> fp32 reductions into the workspace
 //                      accumulator (one 128-byte run per warp and row);
 //   bwd_dq    fp32 dQ accumulator -> bf16.
 // Every MMA runs on fp16 operands: the fp16 copies of Q, K, V, dO made by the pre-pass
@@ -26,9 +28,8 @@
 // significand bits, which the long dK/dQ sums need.  P is formed as scale * P (the scale
 // folded into the exponent), so dS, dQ^T and dK come out scaled and dV is divided by the
 // scale once at the end.
-// TMEM (512 columns): S^T [0,128) -> dQ^T (rows 0-63 at [0,64), 64-127 at [64,128));
-// dP^T [128,256) -> P^T of warpgroup w at [128+32w, 128+32w+16); dV [256,256+D),
-// dK [256+D, 256+2D).
+// TMEM (512 columns): region X at [128X, 128X+128): S^T [0,64) -> dQ^T; dP^T [64,128) ->
+// P^T of warpgroup w2 at [64+32 w2, 64+32 w2+16).  dV [256,256+D), dK [256+D, 256+2D).
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -38,24 +39,26 @@ namespace uly {
 namespace {
 
 constexpr int BN = 128;   // keys per CTA
-constexpr int BM = 128;   // query rows per item
-constexpr int NST = 2;    // Q/dO stages
-constexpr int kCompute = 512;                 // 16 warps
+constexpr int BMI = 64;   // query rows per item
+constexpr int NST = 4;    // Q/dO stages
+constexpr int kRegionThreads = 256;          // 8 warps per TMEM region
 constexpr int kTmaWarp = 16, kMmaWarp = 17;
 constexpr int kThreads = 576;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kBox = 128 * 128;   // [128 rows][128 bytes] swizzle atom column
+constexpr int kBox = 128 * 128;   // [128 rows][128 bytes]
+constexpr int kBox64 = 64 * 128;  // [64 rows][128 bytes]
 
 template <int D>
 struct BwdLayout {
   static constexpr int kKV = (D / 64) * kBox;     // a [128][D] tile
+  static constexpr int kItem = (D / 64) * kBox64; // a [64][D] tile
   static constexpr int kK = 0;                    // K: two atoms (the second zero if D = 64)
   static constexpr int kV = 2 * kBox;
   static constexpr int kQ = kV + kKV;             // [NST]
-  static constexpr int kDO = kQ + NST * kKV;      // [NST]
-  static constexpr int kDS = kDO + NST * kKV;     // fp16 [128 keys][128 rows], two atoms
-  static constexpr int kRow = kDS + 2 * kBox;     // [NST][256] fp32: lse*log2e | D
-  static constexpr int kBar = kRow + NST * 256 * 4;
+  static constexpr int kDO = kQ + NST * kItem;    // [NST]
+  static constexpr int kDS = kDO + NST * kItem;   // [2] fp16 [128 keys][64 rows]
+  static constexpr int kRow = kDS + 2 * kBox;     // [NST][128] fp32: lse terms | D
+  static constexpr int kBar = kRow + NST * 128 * 4;
   static constexpr int kBytes = kBar + 256;
 };
 
@@ -71,9 +74,6 @@ struct BwdArgs {
   uint64_t limit_ns;
 };
 
-__device__ __forceinline__ void red_add(float* addr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
 __device__ __forceinline__ void red_add4(float* addr, float x, float y, float z, float w) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(x), "f"(y),
                "f"(z), "f"(w)
@@ -98,6 +98,15 @@ __device__ __forceinline__ void quad_transpose(float (&x)[4], int lane) {
   x[3] = hi ? y3 : r1;
 }
 
+
+// Item -> (first query row, local query head): the 64-row query tiles that see this key
+// block (from the diagonal on) and, within a tile, the group's heads.
+__device__ __forceinline__ void item_coords(int it, int nb, int gg, int group, int& q0, int& hh) {
+  const int qi = it / group;
+  q0 = nb * BN + qi * BMI;
+  hh = gg * group + (it - qi * group);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -114,24 +123,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 0;
   uint64_t* qd_full = bars + 1;              // [NST]
   uint64_t* qd_empty = bars + 1 + NST;       // [NST]
-  uint64_t* s_full = bars + 1 + 2 * NST;
-  uint64_t* p_full = s_full + 1;
-  uint64_t* dq_full = s_full + 2;
-  uint64_t* dq_free = s_full + 3;
-  uint64_t* acc_done = s_full + 4;
-  uint64_t* drain = s_full + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 6);
+  uint64_t* s_full = bars + 1 + 2 * NST;     // [2] per region
+  uint64_t* p_full = s_full + 2;             // [2]
+  uint64_t* dq_full = s_full + 4;            // [2]
+  uint64_t* dq_free = s_full + 6;            // [2]
+  uint64_t* acc_done = s_full + 8;
+  uint64_t* drain = s_full + 9;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 10);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-  volatile int* decision = abort_flag + 1;   // [2]: outcomes of the compute group's waits
+  volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int per_rank = a.gl * a.nkb;
   const int r = blockIdx.x / per_rank;
   const int rem = blockIdx.x - r * per_rank;
   const int gg = rem / a.nkb;
-  const int nb = rem - gg * a.nkb;             // key block; nb = 0 (most work) first
-  const int nq = (a.S + BM - 1) / BM;
-  const int n_items = a.group * (nq - nb);     // (query tile, head of the group) pairs
+  const int nb = rem - gg * a.nkb;                         // key block; 0 (most work) first
+  const int nqi = (a.S - nb * BN + BMI - 1) / BMI;         // 64-row query tiles that see it
+  const int n_items = a.group * nqi;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -139,10 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qd_full[i], 1);
       mbar_init(&qd_empty[i], 1);
     }
-    mbar_init(s_full, 1);
-    mbar_init(p_full, 1);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], 1);
+      mbar_init(&dq_full[i], 1);
+      mbar_init(&dq_free[i], 1);
+    }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -159,7 +170,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const WaitCtl wc{a.status, abort_flag, a.limit_ns};
 
   if (warp == kTmaWarp) {
-    // TMA for K, V and every item's Q, dO; the whole warp stages the item's row terms.
+    // TMA for K, V and every item's Q, dO (fp16 copies); the whole warp stages the item's
+    // row terms (lse * log2e - log2(scale), and D) next to them.
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
@@ -177,26 +189,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_items; ++it) {
       const int st = it % NST;
       const uint32_t ph = (it / NST) & 1;
-      const int i = nb + it / a.group;
-      const int hh = gg * a.group + it % a.group;
+      int q0, hh;
+      item_coords(it, nb, gg, a.group, q0, hh);
       if (it >= NST && !__all_sync(0xffffffffu, mbar_wait(&qd_empty[st], ph ^ 1, wc))) break;
-      float* rw = rows + st * 256;
+      float* rw = rows + st * 128;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
+      for (int e = 0; e < 2; ++e) {
         const int qc = lane + 32 * e;
-        const int qg = i * BM + qc;
+        const int qg = q0 + qc;
         const size_t idx = ((size_t)r * a.hl + hh) * a.S + qg;
         rw[qc] = qg < a.S ? a.lse[idx] * 1.4426950408889634f - a.log2_scale : INFINITY;
-        rw[128 + qc] = qg < a.S ? a.delta[idx] : 0.f;
+        rw[64 + qc] = qg < a.S ? a.delta[idx] : 0.f;
       }
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kKV);
+        mbar_arrive_expect_tx(&qd_full[st], 2 * L::kItem);
         for (int b = 0; b < D / 64; ++b) {
-          tma_load_4d(smem + L::kQ + st * L::kKV + b * kBox, &tm_q, &qd_full[st], 64 * b, hh,
-                      i * BM, r);
-          tma_load_4d(smem + L::kDO + st * L::kKV + b * kBox, &tm_do, &qd_full[st], 64 * b, hh,
-                      i * BM, r);
+          tma_load_4d(smem + L::kQ + st * L::kItem + b * kBox64, &tm_q, &qd_full[st], 64 * b,
+                      hh, q0, r);
+          tma_load_4d(smem + L::kDO + st * L::kItem + b * kBox64, &tm_do, &qd_full[st], 64 * b,
+                      hh, q0, r);
         }
       }
       ++issued;
@@ -208,119 +220,132 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(BN, BM, false, false);   // S^T, dP^T
-      constexpr uint32_t id_q = idesc_f16(128, 64, true, true);    // dQ^T halves
-      constexpr uint32_t id_kv = idesc_f16(BN, D, false, true);    // dV, dK
+      constexpr uint32_t id_s = idesc_f16(BN, BMI, false, false);  // S^T, dP^T (N = 64)
+      constexpr uint32_t id_q = idesc_f16(128, BMI, true, true);   // dQ^T (M = d, N = 64)
+      constexpr uint32_t id_kv = idesc_f16(BN, D, false, true);    // dV, dK (K = 64 rows)
       // Descriptors are built once; a K-step adds its byte offset / 16 to the address
       // field (no carry: every smem address here is below 2^18).
-      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);      // K-major
+      const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
       const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
-      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), kBox, 1024);   // MN-major
-      const uint64_t dDS_mn = sdesc_sw128(smem_u32(smem + L::kDS), kBox, 1024);
-      const uint64_t dDS_k = sdesc_sw128(smem_u32(smem + L::kDS), 16, 1024);
-      bool alive = mbar_wait(kv_full, 0, wc);
-      for (int it = 0; alive && it < n_items; ++it) {
-        const int st = it % NST;
-        const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kKV);
-        const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kKV);
-        const uint64_t dQ_k = sdesc_sw128(sQ, 16, 1024), dDO_k = sdesc_sw128(sDO, 16, 1024);
-        const uint64_t dQ_mn = sdesc_sw128(sQ, kBox, 1024), dDO_mn = sdesc_sw128(sDO, kBox, 1024);
-        if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) break;
-        if (it >= 1 && !mbar_wait(dq_free, (it - 1) & 1, wc)) break;
+      const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), kBox, 1024);
+      auto mma1 = [&](int it) -> bool {
+        const int X = it & 1, st = it % NST;
+        if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) return false;
+        if (it >= 2 && !mbar_wait(&dq_free[X], ((it - 2) >> 1) & 1, wc)) return false;
         tc_fence_after();
+        const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + L::kQ + st * L::kItem), 16, 1024);
+        const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO + st * L::kItem), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
-          mma_ss(tbase + 0, dK_k + off, dQ_k + off, id_s, kk > 0 ? 1u : 0u);
+          const uint32_t offa = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+          const uint32_t offb = ((kk / 4) * kBox64 + (kk % 4) * 32) >> 4;
+          mma_ss(tbase + 128 * X, dK_k + offa, dQ_k + offb, id_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
-          mma_ss(tbase + 128, dV_k + off, dDO_k + off, id_s, kk > 0 ? 1u : 0u);
+          const uint32_t offa = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+          const uint32_t offb = ((kk / 4) * kBox64 + (kk % 4) * 32) >> 4;
+          mma_ss(tbase + 128 * X + 64, dV_k + offa, dDO_k + offb, id_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
-        if (!mbar_wait(p_full, it & 1, wc)) break;
+        mma_commit(&s_full[X]);
+        return true;
+      };
+      auto mma2 = [&](int it) -> bool {
+        const int X = it & 1, st = it % NST;
+        if (!mbar_wait(&p_full[X], (it >> 1) & 1, wc)) return false;
         tc_fence_after();
-        // dQ^T first: its read-out overlaps the dV and dK MMAs.
+        const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kItem);
+        const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kItem);
+        const uint32_t sDS = smem_u32(smem + L::kDS + X * kBox);
+        const uint64_t dQ_mn = sdesc_sw128(sQ, kBox64, 1024), dDO_mn = sdesc_sw128(sDO, kBox64, 1024);
+        const uint64_t dDS_mn = sdesc_sw128(sDS, kBox, 1024), dDS_k = sdesc_sw128(sDS, 16, 1024);
+        // dQ^T (over this region's S^T columns) first: its read-out overlaps dV and dK.
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tbase + 128 * X, dK_mn + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), id_q,
+                 kk > 0 ? 1u : 0u);
+        mma_commit(&dq_full[X]);
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tbase + 64 * h, dK_mn + ((kk * 2048) >> 4),
-                   dDS_mn + ((h * kBox + kk * 2048) >> 4), id_q, kk > 0 ? 1u : 0u);
-        mma_commit(dq_full);
-#pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ts(tbase + 256, tbase + 128 + 32 * (kk / 2) + 8 * (kk % 2),
+        for (int kk = 0; kk < BMI / 16; ++kk)
+          mma_ts(tbase + 256, tbase + 128 * X + 64 + 32 * (kk / 2) + 8 * (kk % 2),
                  dDO_mn + ((kk * 2048) >> 4), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < BM / 16; ++kk)
-          mma_ss(tbase + 256 + D, dDS_k + (((kk / 4) * kBox + (kk % 4) * 32) >> 4),
-                 dQ_mn + ((kk * 2048) >> 4), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BMI / 16; ++kk)
+          mma_ss(tbase + 256 + D, dDS_k + ((kk * 32) >> 4), dQ_mn + ((kk * 2048) >> 4), id_kv,
+                 (it > 0 || kk > 0) ? 1u : 0u);
         mma_commit(&qd_empty[st]);
+        return true;
+      };
+      bool alive = mbar_wait(kv_full, 0, wc);
+      for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma1(it);
+      for (int it = 0; alive && it < n_items; ++it) {
+        alive = mma2(it);
+        if (alive && it + 2 < n_items) alive = mma1(it + 2);
       }
       if (alive) mma_commit(acc_done);
       mma_commit(drain);
       mbar_drain(drain, 0, a.limit_ns);
     }
   } else {
-    // 16 compute warps.  Warpgroup w = warp / 4 owns query columns [32w, 32w+32) (and, for
-    // the dQ read-out, the same rows); warp % 4 selects the TMEM lane quarter.
-    const int w = warp / 4;
+    // 16 element-wise warps: warps [8X, 8X+8) serve TMEM region X (items X, X+2, ...);
+    // within a region, warpgroup w2 owns query columns [32 w2, 32 w2 + 32) and warp % 4
+    // selects the TMEM lane quarter (= key rows, and d for the dQ^T read-out).
+    const int X = warp / 8;
+    const int w2 = (warp / 4) % 2;
     const int quarter = warp % 4;
-    const int row = quarter * 32 + lane;           // key row (and d for dQ^T)
+    const int row = quarter * 32 + lane;
     const int key_g = nb * BN + row;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t treg = tbase + lane_off + 128 * X;
     const float sl2 = a.scale_log2;
-    uint8_t* ds_row = smem + L::kDS + (w / 2) * kBox + row * 128;
-    // Warp 0 waits on the mbarrier; the other fifteen sleep in a named barrier (no issue
-    // slots) and read the outcome it left, so all of them decide alike.
-    const bool leader = warp == 0;
+    uint8_t* ds_row = smem + L::kDS + X * kBox + row * 128;
+    // The region's first warp waits on the mbarrier; the other seven sleep in a named
+    // barrier (no issue slots) and read the outcome it left, so they all decide alike.
+    const bool leader = (warp % 8) == 0;
     int n_waits = 0;
     auto group_wait = [&](uint64_t* bar, uint32_t parity) -> bool {
-      volatile int* slot = decision + (n_waits & 1);
+      volatile int* slot = decision + 2 * X + (n_waits & 1);
       if (leader) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(bar, parity, wc));
         if (lane == 0) *slot = got ? 1 : 0;
       }
-      named_bar_sync(1, kCompute);
+      named_bar_sync(1 + X, kRegionThreads);
       ++n_waits;
       return *slot != 0;
     };
-    // Every compute thread has finished and fenced its writes; one thread arrives.
+    // All threads of the region have finished (their own TMEM/smem writes fenced); one
+    // thread then arrives for the whole region.
     auto group_arrive = [&](uint64_t* bar) {
-      named_bar_sync(1, kCompute);
+      named_bar_sync(1 + X, kRegionThreads);
       if (leader && lane == 0) mbar_arrive(bar);
     };
     bool ok = true;
-    for (int it = 0; ok && it < n_items; ++it) {
-      const int st = it % NST;
-      const int i = nb + it / a.group;
-      const int hh = gg * a.group + it % a.group;
-      const int q0 = i * BM;
-      const float* rw = rows + st * 256;
-      ok = group_wait(s_full, it & 1);
+    for (int it = X; ok && it < n_items; it += 2) {
+      const int u = it >> 1, st = it % NST;
+      int q0, hh;
+      item_coords(it, nb, gg, a.group, q0, hh);
+      const float* rw = rows + st * 128;
+      ok = group_wait(&s_full[X], u & 1);
       if (!ok) break;
       tc_fence_after();
-      const bool need_mask = (i == nb) || (q0 + BM > a.S) || (nb * BN + BN > a.S);
+      const bool need_mask = (q0 < nb * BN + BN) || (q0 + BMI > a.S) || (nb * BN + BN > a.S);
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t sv[16], dp[16], pk[8], dk[8];
         float lse2[16], dlt[16];
-        const float4* l4 = reinterpret_cast<const float4*>(rw + 32 * w + 16 * c);
-        const float4* d4 = reinterpret_cast<const float4*>(rw + 128 + 32 * w + 16 * c);
+        const float4* l4 = reinterpret_cast<const float4*>(rw + 32 * w2 + 16 * c);
+        const float4* d4 = reinterpret_cast<const float4*>(rw + 64 + 32 * w2 + 16 * c);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float4 x = l4[e], y = d4[e];
           lse2[4 * e] = x.x; lse2[4 * e + 1] = x.y; lse2[4 * e + 2] = x.z; lse2[4 * e + 3] = x.w;
           dlt[4 * e] = y.x; dlt[4 * e + 1] = y.y; dlt[4 * e + 2] = y.z; dlt[4 * e + 3] = y.w;
         }
-        tmem_ld16x2(tbase + lane_off + 32 * w + 16 * c, tbase + lane_off + 128 + 32 * w + 16 * c,
-                    sv, dp);
+        tmem_ld16x2(treg + 32 * w2 + 16 * c, treg + 64 + 32 * w2 + 16 * c, sv, dp);
         if (need_mask) {
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
-            const int qg = q0 + 32 * w + 16 * c + e;
+            const int qg = q0 + 32 * w2 + 16 * c + e;
             if (!(key_g <= qg && qg < a.S && key_g < a.S)) lse2[e] = INFINITY;  // p = 0
           }
         }
@@ -340,13 +365,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // P^T over this warpgroup's own dP^T columns (read above, nobody else reads them)
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
-                tbase + lane_off + 128 + 32 * w + 8 * c),
+                treg + 64 + 32 * w2 + 8 * c),
             "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3]), "r"(pk[4]), "r"(pk[5]), "r"(pk[6]),
             "r"(pk[7])
             : "memory");
 #pragma unroll
         for (int u4 = 0; u4 < 2; ++u4) {
-          const int chunk = (w % 2) * 4 + c * 2 + u4;
+          const int chunk = w2 * 4 + c * 2 + u4;
           *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (row & 7)) * 16)) =
               make_uint4(dk[4 * u4], dk[4 * u4 + 1], dk[4 * u4 + 2], dk[4 * u4 + 3]);
         }
@@ -354,42 +379,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tmem_st_wait();
       tc_fence_before();
-      group_arrive(p_full);
-      // While dV and dK run: read dQ^T out (already scaled, see the row terms).
-      ok = group_wait(dq_full, it & 1);
+      group_arrive(&p_full[X]);
+      // dQ^T of this item (already scaled) -> the workspace accumulator
+      ok = group_wait(&dq_full[X], u & 1);
       if (!ok) break;
       tc_fence_after();
-      // dQ^T to registers, hand the TMEM columns back at once (the next item's MMA1
-      // writes them), then issue the reductions from registers while MMA1 runs.
+      // dQ^T to registers, hand the region's columns back at once (MMA1 of item it+2
+      // writes them), then the reductions from registers.
       uint32_t v[32];
       const bool has_d = quarter * 32 < D;   // warp-uniform: lanes are d = 32*quarter + lane
-      if (has_d) tmem_ld32(tbase + lane_off + 32 * w, v);
+      if (has_d) tmem_ld32(treg + 32 * w2, v);
       tc_fence_before();
-      group_arrive(dq_free);
+      group_arrive(&dq_free[X]);
       if (has_d) {
         // After a 4 x 4 transpose within each group of 4 lanes, lane 4g + b holds d values
         // 32*quarter + 4g .. +3 of query row 4c + b: one 16-byte vector reduction each.
         const int g4 = lane >> 2, b4 = lane & 3;
-        float* ptr = a.dq_acc + (((size_t)r * a.S + q0 + 32 * w + b4) * a.hl + hh) * D +
+        float* ptr = a.dq_acc + (((size_t)r * a.S + q0 + 32 * w2 + b4) * a.hl + hh) * D +
                      32 * quarter + 4 * g4;
         const int rs = a.hl * D;
-        const bool full = q0 + 32 * w + 32 <= a.S;
+        const bool full = q0 + 32 * w2 + 32 <= a.S;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           float x[4] = {__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])};
           quad_transpose(x, lane);
-          if (full || q0 + 32 * w + 4 * c + b4 < a.S)
+          if (full || q0 + 32 * w2 + 4 * c + b4 < a.S)
             red_add4(ptr + 4 * c * rs, x[0], x[1], x[2], x[3]);
         }
       }
     }
-    // dV (warpgroups 0, 1) and dK (2, 3) of this key block.
+    // dV (warps 0-7) and dK (8-15) of this key block, once every MMA has finished.
     if (ok && n_items > 0) ok = __all_sync(0xffffffffu, mbar_wait(acc_done, 0, wc));
     if (ok && n_items > 0) {
       tc_fence_after();
-      const int which = w / 2;            // 0: dV, 1: dK
-      const int half = w % 2;             // columns [32*half*(D/64), ...)
+      const int which = warp / 8;         // 0: dV, 1: dK
+      const int half = w2;                // columns [half * D/2, (half + 1) * D/2)
       __nv_bfloat16* dst = (which ? a.dk : a.dv) + (((size_t)r * a.S + key_g) * a.gl + gg) * D;
       const float mul = which ? 1.f : 1.f / a.scale;   // the dV sums carry the scale
 #pragma unroll 1
@@ -534,8 +559,8 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   const uint64_t dk4[4] = {(uint64_t)D, (uint64_t)gl, (uint64_t)p.S, (uint64_t)p.P};
   const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)gl * D * 2, (uint64_t)p.S * gl * D * 2};
   // the maps read the fp16 copies (TMA moves 16-bit elements either way)
-  if (!make_tmap_4d_bf16(&tq, q16, dq4, sq, 64, BM, &err) ||
-      !make_tmap_4d_bf16(&tdo, do16, dq4, sq, 64, BM, &err) ||
+  if (!make_tmap_4d_bf16(&tq, q16, dq4, sq, 64, BMI, &err) ||
+      !make_tmap_4d_bf16(&tdo, do16, dq4, sq, 64, BMI, &err) ||
       !make_tmap_4d_bf16(&tk, k16, dk4, sk, 64, BN, &err) ||
       !make_tmap_4d_bf16(&tv, v16, dk4, sk, 64, BN, &err))
     return cudaErrorInvalidValue;
