@@ -159,26 +159,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
       const bool stall = (a.flags & ULY_FLAG_INJECT_STALL) && blockIdx.x == 0;
       bool alive = mbar_wait(q_full, 0, wc);
+      // descriptors built once; K-steps add byte offset / 16 (smem addresses < 2^18)
+      const uint64_t dq0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(smem_u32(smem + L::kV), kBox, 1024);
       auto issue_s = [&](int t, int j) {
-        const uint32_t qa = smem_u32(smem + L::kQ + t * L::kTile);
-        const uint32_t kb = smem_u32(smem + L::kK + (j & 1) * L::kTile);
+        const uint64_t qa = dq0 + ((t * L::kTile) >> 4);
+        const uint64_t kb = dk0 + (((j & 1) * L::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * kBox + (kk % 4) * 32;
-          mma_ss(tbase + t * BN, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
-                 idesc_qk, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+          mma_ss(tbase + t * BN, qa + off, kb + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
       auto issue_pv = [&](int t, int j) -> bool {
         if (!mbar_wait(&p_full[t], j & 1, wc)) return false;
         if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t vb = smem_u32(smem + L::kV + (j & 1) * L::kTile);
+        const uint64_t vb = dv0 + (((j & 1) * L::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tbase + 2 * BN + t * D, tbase + t * BN + kk * 8,
-                 sdesc_sw128(vb + kk * 16 * 128, kBox, 1024), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + 2 * BN + t * D, tbase + t * BN + kk * 8, vb + ((kk * 16 * 128) >> 4),
+                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         return true;
       };
       for (int j = 0; alive && j < n1; ++j) {
@@ -239,11 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (kp > row_g || kp >= a.S) s[c][i] = __float_as_uint(-INFINITY);
           }
       }
-      float mx = -INFINITY;
+      // row max: four independent chains of 3-input max
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(s[c][i]));
+        for (int i = 0; i < 32; i += 2)
+          mq[c] = fmax3(mq[c], __uint_as_float(s[c][i]), __uint_as_float(s[c][i + 1]));
+      const float mx = fmax3(fmaxf(mq[0], mq[1]), mq[2], mq[3]);
       const float m_new = fmaxf(m_used, mx * sl2);
       float alpha = 1.f;
       bool rescale = false;
@@ -254,19 +259,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_used = m_new;
         rescale = true;
       }
-      float sum = 0.f;
+      // p = 2^(s * scale * log2e - m) on pairs: one FFMA2, two MUFU, one FADD2 per pair
+      const uint64_t sc2 = f2_pack(sl2, sl2), nm2 = f2_pack(-m_used, -m_used);
+      uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i]), sl2, -m_used));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(s[c][2 * i + 1]), sl2, -m_used));
-          sum += p0 + p1;
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(s[c][2 * i]), __uint_as_float(s[c][2 * i + 1])),
+                          sc2, nm2),
+                    x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          sum2 = fadd2(sum2, f2_pack(p0, p1));
           pk[i] = pack_bf16x2(p0, p1);
         }
         tmem_st16(ts + 16 * c, pk);
       }
+      float sum_lo, sum_hi;
+      f2_unpack(sum2, sum_lo, sum_hi);
+      const float sum = sum_lo + sum_hi;
       l = l * alpha + sum;
       // tcgen05.ld/st are warp-collective: the whole warp rescales when any row needs it
       // (rows that do not need it have alpha = 1).
