@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qc = lane + 32 * e;
         const int qg = q0 + qc;
         const size_t idx = ((size_t)r * a.hl + hh) * a.S + qg;
-        rw[qc] = qg < a.S ? a.lse[idx] * 1.4426950408889634f - a.log2_scale : INFINITY;
+        rw[qc] = qg < a.S ? a.log2_scale - a.lse[idx] * 1.4426950408889634f : -INFINITY;
         rw[64 + qc] = qg < a.S ? a.delta[idx] : 0.f;
       }
       __syncwarp();
@@ -332,35 +332,43 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < 2; ++c) {
         uint32_t sv[16], dp[16], pk[8], dk[8];
-        float lse2[16], dlt[16];
-        const float4* l4 = reinterpret_cast<const float4*>(rw + 32 * w2 + 16 * c);
-        const float4* d4 = reinterpret_cast<const float4*>(rw + 64 + 32 * w2 + 16 * c);
+        // row terms as packed pairs: nl = log2(scale) - lse*log2e (-inf: masked), dl = D
+        uint64_t nl[8], dl[8];
+        const ulonglong2* l4 = reinterpret_cast<const ulonglong2*>(rw + 32 * w2 + 16 * c);
+        const ulonglong2* d4 = reinterpret_cast<const ulonglong2*>(rw + 64 + 32 * w2 + 16 * c);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float4 x = l4[e], y = d4[e];
-          lse2[4 * e] = x.x; lse2[4 * e + 1] = x.y; lse2[4 * e + 2] = x.z; lse2[4 * e + 3] = x.w;
-          dlt[4 * e] = y.x; dlt[4 * e + 1] = y.y; dlt[4 * e + 2] = y.z; dlt[4 * e + 3] = y.w;
+          const ulonglong2 x = l4[e], y = d4[e];
+          nl[2 * e] = x.x; nl[2 * e + 1] = x.y;
+          dl[2 * e] = y.x; dl[2 * e + 1] = y.y;
         }
         tmem_ld16x2(treg + 32 * w2 + 16 * c, treg + 64 + 32 * w2 + 16 * c, sv, dp);
         if (need_mask) {
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int qg = q0 + 32 * w2 + 16 * c + e;
-            if (!(key_g <= qg && qg < a.S && key_g < a.S)) lse2[e] = INFINITY;  // p = 0
+          for (int i2 = 0; i2 < 8; ++i2) {
+            float n0, n1;
+            f2_unpack(nl[i2], n0, n1);
+            const int qg = q0 + 32 * w2 + 16 * c + 2 * i2;
+            if (!(key_g <= qg && qg < a.S && key_g < a.S)) n0 = -INFINITY;          // p = 0
+            if (!(key_g <= qg + 1 && qg + 1 < a.S && key_g < a.S)) n1 = -INFINITY;
+            nl[i2] = f2_pack(n0, n1);
           }
         }
+        const uint64_t sc2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int j = 2 * i2 + e;
-            const float p = ex2_approx(fmaf(__uint_as_float(sv[j]), sl2, -lse2[j]));
-            pv[e] = p;
-            dv[e] = p * (__uint_as_float(dp[j]) - dlt[j]);
-          }
-          pk[i2] = pack_f16x2_sat(pv[0], pv[1]);
-          dk[i2] = pack_f16x2_sat(dv[0], dv[1]);
+          // P_s = 2^(s scale log2e + nl), dS_s = P_s (dP - D): one FFMA2, FSUB2, FMUL2 per pair
+          float x0, x1;
+          f2_unpack(ffma2(f2_pack(__uint_as_float(sv[2 * i2]), __uint_as_float(sv[2 * i2 + 1])),
+                          sc2, nl[i2]),
+                    x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          const uint64_t d2 = fsub2(f2_pack(__uint_as_float(dp[2 * i2]), __uint_as_float(dp[2 * i2 + 1])),
+                                    dl[i2]);
+          float ds0, ds1;
+          f2_unpack(fmul2(f2_pack(p0, p1), d2), ds0, ds1);
+          pk[i2] = pack_f16x2_sat(p0, p1);
+          dk[i2] = pack_f16x2_sat(ds0, ds1);
         }
         // P^T over this warpgroup's own dP^T columns (read above, nobody else reads them)
         asm volatile(
