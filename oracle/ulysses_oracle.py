@@ -282,3 +282,68 @@ def a2a_volume_bytes(S: int, P: int, H: int, G: int, D: int, elem_bytes: int = 2
     s2h = n * (H + 2 * G) * D * elem_bytes * (P - 1) // P
     h2s = n * H * D * elem_bytes * (P - 1) // P
     return s2h, h2s
+
+
+# ------------------------------------------------------- rest of the block's backward
+def rope_backward(g: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Gradient through rotate-half RoPE: each pair (i, i + D/2) was turned by the angle
+    p * theta^(-2i/D); the gradient turns back by the same angle (the transpose of a
+    rotation).  g: [T][n_heads][D]."""
+    g = np.asarray(g, np.float64)
+    half = g.shape[-1] // 2
+    phi = rope_angles(positions, g.shape[-1], theta)[:, None, :]
+    c, s = np.cos(phi), np.sin(phi)
+    lo, hi = g[..., :half], g[..., half:]
+    return np.concatenate([lo * c + hi * s, hi * c - lo * s], axis=-1)
+
+
+def qkv_projection_backward(x: np.ndarray, w: np.ndarray, dy: np.ndarray):
+    """Gradients of y = x w^T: dx = dy w ([T][hidden]), dw = dy^T x ([C][hidden])."""
+    dy = np.asarray(dy, np.float64)
+    return dy @ np.asarray(w, np.float64), dy.T @ np.asarray(x, np.float64)
+
+
+def head_to_seq_qkv(dq_head, dk_head, dv_head, P: int) -> np.ndarray:
+    """The three head-layout gradients back to the projection layout [S][H + 2G][D]:
+    the inverse of seq_to_head, written as the same rank-to-rank exchange."""
+    S = dq_head.shape[1]
+    parts = [head_to_seq(t, P).reshape(S, -1, t.shape[-1]) for t in (dq_head, dk_head, dv_head)]
+    return np.concatenate(parts, axis=1)
+
+
+def ulysses_block_backward(x, w, do_seq, P: int, H: int, G: int, D: int, theta: float = 0.0,
+                           scale=None):
+    """Training step of one Ulysses block: gradients dx [S][hidden] and dw [C][hidden] of
+    L = sum(o_seq * do_seq), following the forward's steps in reverse:
+      dO seq->head; per-rank attention backward; head->seq of dq, dk, dv; RoPE backward
+      at global positions; projection backward.
+    Returns dx, dw and the intermediate dqkv_seq [S][H + 2G][D]."""
+    x = np.asarray(x, np.float64)
+    S = x.shape[0]
+    _, _, (qkv_seq, q, k, v, _) = ulysses_block_forward(x, w, P, H, G, D, theta, scale)
+    do_seq = np.asarray(do_seq, np.float64).reshape(S, H, D)
+    do_head = np.stack([head for head in _seq_to_head_one(do_seq, P)])
+    dq, dk, dv = [], [], []
+    for r in range(P):
+        a, b, c = causal_attention_bwd(q[r], k[r], v[r], do_head[r], scale)
+        dq.append(a)
+        dk.append(b)
+        dv.append(c)
+    dqkv = head_to_seq_qkv(np.stack(dq), np.stack(dk), np.stack(dv), P)
+    if theta:
+        pos = np.arange(S)
+        dqkv = np.concatenate([rope_backward(dqkv[:, :H + G], pos, theta), dqkv[:, H + G:]],
+                              axis=1)
+    dx, dw = qkv_projection_backward(x, w, dqkv.reshape(S, -1))
+    return dx, dw, dqkv
+
+
+def _seq_to_head_one(x_seq: np.ndarray, P: int):
+    """seq->head of one tensor [S][n][D] -> [P][S][n/P][D] (rank-to-rank exchange)."""
+    S, n, D = x_seq.shape
+    per, hl = S // P, n // P
+    out = np.empty((P, S, hl, D), x_seq.dtype)
+    for r in range(P):
+        for r2 in range(P):
+            out[r2, r * per:(r + 1) * per] = x_seq[r * per:(r + 1) * per, r2 * hl:(r2 + 1) * hl]
+    return out

@@ -347,3 +347,57 @@ def test_generator_is_deterministic_and_normal():
     assert abs(x.mean()) < 0.02 and abs(x.std() - 1) < 0.02
     w = synthetic.bf16_to_f64(synthetic.normal_bf16(0, 1, (1 << 16,), std=0.02))
     assert abs(w.std() - 0.02) < 0.001
+
+
+# ------------------------------------------------- backward of projection and RoPE
+def test_rope_backward_inverts_and_matches_autograd():
+    D, theta = 16, 500000.0
+    r = _rng(20)
+    x = r.standard_normal((9, 3, D))
+    pos = np.array([0, 1, 5, 77, 1000, 4095, 65535, 131071, 1 << 20])
+    assert np.allclose(O.rope_backward(O.apply_rope(x, pos, theta), pos, theta), x,
+                       rtol=0, atol=1e-12)
+    g = r.standard_normal(x.shape)
+    half = D // 2
+    tx = torch.from_numpy(x).clone().requires_grad_(True)
+    phi = torch.from_numpy(O.rope_angles(pos, D, theta))[:, None, :]
+    lo, hi = tx[..., :half], tx[..., half:]
+    y = torch.cat([lo * torch.cos(phi) - hi * torch.sin(phi), hi * torch.cos(phi) + lo * torch.sin(phi)], -1)
+    (y * torch.from_numpy(g)).sum().backward()
+    assert np.allclose(O.rope_backward(g, pos, theta), tx.grad.numpy(), rtol=0, atol=1e-12)
+
+
+def test_projection_backward_brute_force():
+    r = _rng(21)
+    x, w, dy = r.standard_normal((5, 4)), r.standard_normal((6, 4)), r.standard_normal((5, 6))
+    dx, dw = O.qkv_projection_backward(x, w, dy)
+    for s in range(5):
+        for k in range(4):
+            assert abs(dx[s, k] - sum(dy[s, c] * w[c, k] for c in range(6))) < 1e-12
+    for c in range(6):
+        for k in range(4):
+            assert abs(dw[c, k] - sum(dy[s, c] * x[s, k] for s in range(5))) < 1e-12
+
+
+def test_block_backward_matches_torch_autograd():
+    """The whole block's training gradients against torch float64 autograd of the same
+    forward written in torch (projection, RoPE, unsharded causal GQA attention)."""
+    S, hidden, H, G, D, P, theta = 32, 16, 4, 2, 8, 2, 10000.0
+    r = _rng(22)
+    x, w = r.standard_normal((S, hidden)), 0.3 * r.standard_normal(((H + 2 * G) * D, hidden))
+    do = r.standard_normal((S, H * D))
+    dx, dw, _ = O.ulysses_block_backward(x, w, do, P, H, G, D, theta)
+    tx, tw = (torch.from_numpy(a).clone().requires_grad_(True) for a in (x, w))
+    y = (tx @ tw.T).reshape(S, H + 2 * G, D)
+    half = D // 2
+    phi = torch.from_numpy(O.rope_angles(np.arange(S), D, theta))[:, None, :]
+
+    def rope(t):
+        lo, hi = t[..., :half], t[..., half:]
+        return torch.cat([lo * torch.cos(phi) - hi * torch.sin(phi), hi * torch.cos(phi) + lo * torch.sin(phi)], -1)
+
+    q, k, v = rope(y[:, :H]), rope(y[:, H:H + G]), y[:, H + G:]
+    o = _torch_attention(q, k, v, H, G)
+    (o.reshape(S, H * D) * torch.from_numpy(do)).sum().backward()
+    assert np.allclose(dx, tx.grad.numpy(), rtol=0, atol=1e-10)
+    assert np.allclose(dw, tw.grad.numpy(), rtol=0, atol=1e-10)
