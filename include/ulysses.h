@@ -164,6 +164,26 @@ uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void *q, const void *k,
 uly_status ulysses_head_to_seq(uly_plan plan, const void *x_head, int n_heads, void *x_seq,
                                void *stream);
 
+/* Rest of the block's training step (the pages' method is for training, Hugging Face post
+ * para 1; these gradients mirror the forward steps above in reverse).
+ *
+ * head->seq all-to-all of the attention gradients back into the projection layout:
+ * dq [P][S][H/P][D], dk, dv [P][S][G/P][D] -> dqkv_seq [P][S/P][H + 2G][D] (= [S][C]),
+ * the exact inverse of ulysses_seq_to_head's permutation.  apply_rope != 0 (needs
+ * rope_theta > 0) applies the RoPE backward to the q and k parts: each pair (i, i + D/2)
+ * at global position s is turned back by s * theta^(-2i/D) (the transpose of the forward
+ * rotation), in fp32, rounded once to bf16.  Without RoPE it moves bits unchanged. */
+uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void *dq, const void *dk,
+                                   const void *dv, int apply_rope, void *dqkv_seq,
+                                   void *stream);
+
+/* Backward of ulysses_qkv_proj: dx[s][k] = sum_c dqkv[s][c] w[c][k] (bf16 [S][hidden], RNE)
+ * and dw[c][k] = sum_s dqkv[s][c] x[s][k] (fp32 [C][hidden], summed over all S tokens of
+ * all shards, as the shared weight's gradient); fp32 accumulation.  Either output may be
+ * NULL to skip it. */
+uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void *x, const void *w,
+                                const void *dqkv, void *dx, float *dw, void *stream);
+
 /* Synchronises `stream`, reads the plan's device status word, clears it and returns it
  * (ULY_OK, or e.g. ULY_ERR_TIMEOUT).  ULY_ERR_CUDA if the synchronisation itself fails. */
 uly_status ulysses_sync_status(uly_plan plan, void *stream);

@@ -22,7 +22,7 @@ _STATUS_NAMES = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED"
 EXPORTED = ("ulysses_plan", "ulysses_plan_destroy", "ulysses_workspace_bytes",
             "ulysses_qkv_proj", "ulysses_seq_to_head", "ulysses_seq_to_head_heads",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc",
-            "ulysses_head_to_seq",
+            "ulysses_head_to_seq", "ulysses_head_to_seq_qkv", "ulysses_qkv_proj_bwd",
             "ulysses_sync_status", "ulysses_bytes_moved", "ulysses_a2a_volume",
             "ulysses_last_error")
 
@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH):
         "ulysses_attn_bwd": ([vp] * 13, i32),
         "ulysses_attn_bwd_noalloc": ([vp] * 12, i32),
         "ulysses_head_to_seq": ([vp, vp, i32, vp, vp], i32),
+        "ulysses_head_to_seq_qkv": ([vp, vp, vp, vp, i32, vp, vp], i32),
+        "ulysses_qkv_proj_bwd": ([vp] * 7, i32),
         "ulysses_sync_status": ([vp, vp], i32),
         "ulysses_bytes_moved": ([vp], u64),
         "ulysses_a2a_volume": ([ctypes.POINTER(UlyConfig), ctypes.POINTER(u64),
@@ -200,6 +202,17 @@ def ulysses_attn_bwd_noalloc(plan, q, k, v, o, lse, d_o, dq, dk, dv, stream=None
 def ulysses_head_to_seq(plan, x_head, n_heads, x_seq, stream=None):
     _check(load_library().ulysses_head_to_seq(plan.handle, _ptr(x_head), int(n_heads),
                                               _ptr(x_seq), _stream(stream)))
+
+
+def ulysses_head_to_seq_qkv(plan, dq, dk, dv, dqkv_seq, apply_rope=False, stream=None):
+    _check(load_library().ulysses_head_to_seq_qkv(plan.handle, _ptr(dq), _ptr(dk), _ptr(dv),
+                                                  1 if apply_rope else 0, _ptr(dqkv_seq),
+                                                  _stream(stream)))
+
+
+def ulysses_qkv_proj_bwd(plan, x, w, dqkv, dx=None, dw=None, stream=None):
+    _check(load_library().ulysses_qkv_proj_bwd(plan.handle, _ptr(x), _ptr(w), _ptr(dqkv),
+                                               _ptr(dx), _ptr(dw), _stream(stream)))
 
 
 def ulysses_sync_status(plan, stream=None) -> int:

@@ -356,6 +356,35 @@ uly_status ulysses_attn_bwd(uly_plan plan, const void* q, const void* k, const v
                   "attn_bwd launch");
 }
 
+uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void* dq, const void* dk, const void* dv,
+                                   int apply_rope, void* dqkv_seq, void* stream) {
+  if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  Plan& p = plan->p;
+  if (p.S == 0) return ULY_OK;
+  if (!dq || !dk || !dv || !dqkv_seq) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(dqkv_seq))
+    return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (apply_rope && !(p.cfg.rope_theta > 0))
+    return fail(ULY_ERR_INVALID_ARG, "apply_rope needs a plan with rope_theta > 0");
+  p.bytes_moved += (uint64_t)p.S * (p.H + 2 * p.G) * p.D * 4;
+  return launched(uly::launch_head_to_seq_qkv(p, dq, dk, dv, apply_rope != 0, dqkv_seq,
+                                              as_stream(stream)),
+                  "head_to_seq_qkv launch");
+}
+
+uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void* x, const void* w, const void* dqkv,
+                                void* dx, float* dw, void* stream) {
+  if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  const Plan& p = plan->p;
+  if (p.S == 0) return ULY_OK;
+  if (!x || !w || !dqkv) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(x) || !aligned16(w) || !aligned16(dqkv) || !aligned16(dx) || !aligned16(dw))
+    return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (p.S > (int64_t(1) << 31) - 1) return fail(ULY_ERR_UNSUPPORTED, "S too large");
+  return launched(uly::launch_qkv_gemm_bwd(p, x, w, dqkv, dx, dw, as_stream(stream)),
+                  "qkv_proj_bwd launch");
+}
+
 uly_status ulysses_sync_status(uly_plan plan, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   cudaError_t e = cudaStreamSynchronize(as_stream(stream));

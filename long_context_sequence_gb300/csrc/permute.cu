@@ -131,6 +131,69 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
   }
 }
 
+// Inverse of seq_to_head for the gradients: dq [P][S][H/P][D], dk, dv [P][S][G/P][D] ->
+// dqkv [S][H + 2G][D], with the RoPE backward on the q and k parts (each pair turned back
+// by its angle: lo' = lo cos + hi sin, hi' = hi cos - lo sin).  Same work units as above.
+template <bool kRope>
+__global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
+    const __nv_bfloat16* __restrict__ dq, const __nv_bfloat16* __restrict__ dk,
+    const __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ out, int64_t S, int P,
+    int H, int G, int D, RopeTab rope) {
+  const int C = H + 2 * G;
+  const int upr = D / 16;
+  const int U = C * upr;
+  const int hq = H / P, hk = G / P;
+  const int64_t n_blocks = (S + kTokensPerBlock - 1) / kTokensPerBlock;
+  for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
+    const int64_t s0 = b * kTokensPerBlock;
+    const int ntok = (int)(S - s0 < kTokensPerBlock ? S - s0 : kTokensPerBlock);
+    for (int w = threadIdx.x; w < ntok * U; w += kThreads) {
+      const int tl = w / U;
+      const int unit = w - tl * U;
+      const int c = unit / upr;
+      const int cu = unit - c * upr;
+      const int64_t s = s0 + tl;
+      const __nv_bfloat16* src;
+      if (c < H) {
+        const int r2 = c / hq, hh = c - r2 * hq;
+        src = dq + (((size_t)r2 * S + s) * hq + hh) * D;
+      } else if (c < H + G) {
+        const int g = c - H, r2 = g / hk, hh = g - r2 * hk;
+        src = dk + (((size_t)r2 * S + s) * hk + hh) * D;
+      } else {
+        const int g = c - H - G, r2 = g / hk, hh = g - r2 * hk;
+        src = dv + (((size_t)r2 * S + s) * hk + hh) * D;
+      }
+      __nv_bfloat16* dst = out + ((size_t)s * C + c) * D;
+      const int e_lo = cu * 8, e_hi = D / 2 + cu * 8;
+      const uint4 raw_lo = ld_stream(src + e_lo), raw_hi = ld_stream(src + e_hi);
+      if (kRope && c < H + G) {
+        float lo[8], hi[8];
+        unpack8(raw_lo, lo);
+        unpack8(raw_hi, hi);
+        const int64_t sh = s / kRopeL;
+        const int sl = (int)(s - sh * kRopeL);
+        const float2* th = rope.hi + sh * rope.half + e_lo;
+        const float2* tl2 = rope.lo + (int64_t)sl * rope.half + e_lo;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float2 a = __ldg(th + i), bb = __ldg(tl2 + i);
+          const float cs = fmaf(a.x, bb.x, -a.y * bb.y);
+          const float sn = fmaf(a.y, bb.x, a.x * bb.y);
+          const float x0 = lo[i], x1 = hi[i];
+          lo[i] = fmaf(x0, cs, x1 * sn);
+          hi[i] = fmaf(x1, cs, -x0 * sn);
+        }
+        st_stream(dst + e_lo, pack8(lo));
+        st_stream(dst + e_hi, pack8(hi));
+      } else {
+        st_stream(dst + e_lo, raw_lo);
+        st_stream(dst + e_hi, raw_hi);
+      }
+    }
+  }
+}
+
 // One tensor of n heads: seq layout [S][n][D] <-> head layout [P][S][n/P][D].
 // Iterates over the seq side (contiguous); the head side is written/read in runs of
 // (n/P) * D elements.
@@ -185,6 +248,21 @@ cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool
     seq_to_head_kernel<false, true><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab);
   else
     seq_to_head_kernel<false, false><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk,
+                                   const void* dv, bool rope, void* out, cudaStream_t st) {
+  const int grid = permute_grid(p, p.S);
+  RopeTab tab{p.rope_hi, p.rope_lo, p.D / 2};
+  auto* a = static_cast<const __nv_bfloat16*>(dq);
+  auto* b = static_cast<const __nv_bfloat16*>(dk);
+  auto* c = static_cast<const __nv_bfloat16*>(dv);
+  auto* o = static_cast<__nv_bfloat16*>(out);
+  if (rope)
+    head_to_seq_qkv_kernel<true><<<grid, kThreads, 0, st>>>(a, b, c, o, p.S, p.P, p.H, p.G, p.D, tab);
+  else
+    head_to_seq_qkv_kernel<false><<<grid, kThreads, 0, st>>>(a, b, c, o, p.S, p.P, p.H, p.G, p.D, tab);
   return cudaGetLastError();
 }
 

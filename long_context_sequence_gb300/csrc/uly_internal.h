@@ -37,8 +37,13 @@ cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool
                                void* k, void* v, cudaStream_t st);
 cudaError_t launch_permute_heads(const Plan& p, const void* in, int n_heads, void* out,
                                  bool to_head, cudaStream_t st);
+cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk,
+                                   const void* dv, bool rope, void* out, cudaStream_t st);
 cudaError_t launch_qkv_gemm(const Plan& p, const void* x, const void* w, void* out,
                             cudaStream_t st);
+// dx = dqkv w (bf16 [S][hidden]) and dw = dqkv^T x (fp32 [C][hidden]); either may be null.
+cudaError_t launch_qkv_gemm_bwd(const Plan& p, const void* x, const void* w, const void* dqkv,
+                                void* dx, float* dw, cudaStream_t st);
 cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v,
                             void* o, void* o_lo, float* lse, cudaStream_t st);
 cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const void* v,
