@@ -104,7 +104,7 @@ def run_reference(args):
         return
     w = WORKLOAD
     S = args.seq or w["S"]
-    rows = 128
+    rows = 1024
     for _ in range(args.warmup):
         oracle_sample(S, w["H"], w["D"], rows)
     flops = secs = 0.0
@@ -216,15 +216,13 @@ def run_ours(args):
     o_seq = torch.empty(sh["o_seq"], dtype=bf, device=dev)
     do = torch.empty(sh["o"], dtype=bf, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dq_seq = torch.empty(sh["o_seq"], dtype=bf, device=dev)
-    dk_seq = torch.empty(sh["kv_seq"], dtype=bf, device=dev)
-    dv_seq = torch.empty(sh["kv_seq"], dtype=bf, device=dev)
+    dqkv_seq = torch.empty(sh["qkv"], dtype=bf, device=dev)
     ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     sid = stream.cuda_stream
     names = ["qkv_proj", "seq_to_head", "attn_fwd", "head_to_seq_o", "seq_to_head_do",
              "attn_bwd", "head_to_seq_grads"]
-    launches_per_step = 1 + 1 + 1 + 1 + 1 + 3 + 3
+    launches_per_step = 1 + 1 + 1 + 1 + 1 + 3 + 1
 
     def step(ev=None):
         def mark(i):
@@ -243,9 +241,7 @@ def run_ours(args):
         mark(5)
         U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid, o_lo=o_lo)
         mark(6)
-        U.ulysses_head_to_seq(plan, dq, H, dq_seq, sid)
-        U.ulysses_head_to_seq(plan, dk, G, dk_seq, sid)
-        U.ulysses_head_to_seq(plan, dv, G, dv_seq, sid)
+        U.ulysses_head_to_seq_qkv(plan, dq, dk, dv, dqkv_seq, apply_rope=True, stream=sid)
         mark(7)
 
     for _ in range(args.warmup):
@@ -303,7 +299,7 @@ def run_ours(args):
         hdo = torch.empty(sh["o_seq"], dtype=bf, pin_memory=True)
         hx.copy_(x)
         hdo.copy_(do_seq)
-        outs = [o_seq, dq_seq, dk_seq, dv_seq]
+        outs = [o_seq, dqkv_seq]
         houts = [torch.empty(t.shape, dtype=bf, pin_memory=True) for t in outs]
         h2d = hx.numel() * 2 + hdo.numel() * 2
         d2h = sum(t.numel() * 2 for t in outs)
@@ -329,9 +325,36 @@ def run_ours(args):
         e2e = {"value": job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOPS",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
+    # rest of the block's training step, timed on its own: the QKV projection backward
+    # (dx = dqkv w, dw = dqkv^T x) on the gradient the step just produced
+    pbwd = None
+    if not args.no_proj_bwd:
+        dx = torch.empty(sh["x"], dtype=bf, device=dev)
+        dw = torch.empty(sh["w"], dtype=torch.float32, device=dev)
+        for _ in range(args.warmup):
+            U.ulysses_qkv_proj_bwd(plan, x, wq, dqkv_seq, dx, dw, sid)
+        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for e in pev:
+            e[0].record(stream)
+            U.ulysses_qkv_proj_bwd(plan, x, wq, dqkv_seq, dx, None, sid)
+            e[1].record(stream)
+            U.ulysses_qkv_proj_bwd(plan, x, wq, dqkv_seq, None, dw, sid)
+            e[2].record(stream)
+        torch.cuda.synchronize()
+        st = U.ulysses_sync_status(plan, sid)
+        if st != U.ULY_OK:
+            raise RuntimeError("device status %d: %s" % (st, U.ulysses_last_error()))
+        dx_ms = sum(e[0].elapsed_time(e[1]) for e in pev) / len(pev)
+        dw_ms = sum(e[1].elapsed_time(e[2]) for e in pev) / len(pev)
+        gf = 2.0 * S * hidden * C
+        pbwd = {"dx_ms": dx_ms, "dw_ms": dw_ms, "dx_tflops": gf / (dx_ms * 1e-3) / 1e12,
+                "dw_tflops": gf / (dw_ms * 1e-3) / 1e12,
+                "block_train_step_ms": ms_step + dx_ms + dw_ms}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        f, s, desc = oracle_sample(S, H, D, 512)
+        f, s, desc = oracle_sample(S, H, D, 6144)
         cpu = {"value": f / s / 1e12, "unit": "TFLOPS", "cores": host_cores(), "kind": "oracle",
                "sample": desc, "seconds": s}
 
@@ -357,6 +380,7 @@ def run_ours(args):
             "seq_to_head_gbs": s2h_gbs, "peaks": peaks, "peaks_source": peak_kind,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+            "qkv_proj_bwd": pbwd,
         }
         print(json.dumps(line))
     plan.close()
@@ -372,6 +396,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seq", type=int, default=0, help="override S (quick checks only)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-proj-bwd", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.seq:
