@@ -26,7 +26,11 @@ Points the pages leave open are read as follows (the plainest reading):
   * RoPE is the rotate-half form: for pair (i, i + D/2) at position p the pair is rotated
     by angle p * theta^(-2i/D), positions are global token indices;
   * the projection weight has nn.Linear layout [(H + 2G) * D][hidden], columns ordered
-    q heads, then k heads, then v heads.
+    q heads, then k heads, then v heads;
+  * the block ends with the output projection of the restored shard, weight wo in
+    nn.Linear layout [hidden][H * D], input columns ordered head-major (h * D + d);
+  * the training step's loss is L = sum(output * upstream gradient); its gradients follow
+    the forward steps in reverse (RoPE backward = rotation by the negative angle).
 
 Pins (tests/test_oracle.py): brute-force loops on tiny inputs, a hand-worked attention
 example and a hand-written all-to-all index table under tests/golden/, closed forms
@@ -347,3 +351,43 @@ def _seq_to_head_one(x_seq: np.ndarray, P: int):
         for r2 in range(P):
             out[r2, r * per:(r + 1) * per] = x_seq[r * per:(r + 1) * per, r2 * hl:(r2 + 1) * hl]
     return out
+
+
+# ------------------------------------------------------------------ output projection
+# After the second all-to-all restores the sequence sharding [UT para 2], the attention
+# block ends, as every transformer attention block does, with its output projection
+# y = o wo^T, o the rank's shard [S/P][H * D] and wo the nn.Linear weight [hidden][H * D].
+def output_projection(o_seq: np.ndarray, wo: np.ndarray) -> np.ndarray:
+    """y[t][j] = sum_c o[t][c] wo[j][c] with c = h * D + d; o_seq: [..][H][D] tokens."""
+    o = np.asarray(o_seq, np.float64)
+    o = o.reshape(-1, o.shape[-2] * o.shape[-1])
+    return o @ np.asarray(wo, np.float64).T
+
+
+def output_projection_backward(o_seq: np.ndarray, wo: np.ndarray, dy: np.ndarray):
+    """Gradients of y = o wo^T: do = dy wo ([T][H * D]) and dwo = dy^T o ([hidden][H * D])."""
+    o = np.asarray(o_seq, np.float64)
+    o = o.reshape(-1, o.shape[-2] * o.shape[-1])
+    dy = np.asarray(dy, np.float64)
+    return dy @ np.asarray(wo, np.float64), dy.T @ o
+
+
+def ulysses_layer_forward(x, w, wo, P: int, H: int, G: int, D: int, theta: float = 0.0,
+                          scale=None):
+    """The whole attention block: ulysses_block_forward, then each rank's output projection
+    of its restored shard.  Returns y [S][hidden], lse and o_seq [P][S/P][H][D]."""
+    o_seq, lse, _ = ulysses_block_forward(x, w, P, H, G, D, theta, scale)
+    y = np.concatenate([output_projection(o_seq[r], wo) for r in range(P)], axis=0)
+    return y, lse, o_seq
+
+
+def ulysses_layer_backward(x, w, wo, dy, P: int, H: int, G: int, D: int, theta: float = 0.0,
+                           scale=None):
+    """Gradients of L = sum(y * dy) for the whole block: the output projection's backward
+    per rank gives dO in the sequence layout and dwo (summed over all ranks' tokens), then
+    ulysses_block_backward.  Returns dx, dw, dwo and dO_seq [S][H][D]."""
+    o_seq, _, _ = ulysses_block_forward(x, w, P, H, G, D, theta, scale)
+    S = np.asarray(x).shape[0]
+    do_seq, dwo = output_projection_backward(o_seq.reshape(S, H, D), wo, dy)
+    dx, dw, _ = ulysses_block_backward(x, w, do_seq, P, H, G, D, theta, scale)
+    return dx, dw, dwo, do_seq.reshape(S, H, D)

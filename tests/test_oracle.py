@@ -401,3 +401,76 @@ def test_block_backward_matches_torch_autograd():
     (o.reshape(S, H * D) * torch.from_numpy(do)).sum().backward()
     assert np.allclose(dx, tx.grad.numpy(), rtol=0, atol=1e-10)
     assert np.allclose(dw, tw.grad.numpy(), rtol=0, atol=1e-10)
+
+
+def test_output_projection_brute_force():
+    """y[t][j] = sum over heads h and dims d of o[t][h][d] wo[j][h*D + d], written as loops;
+    the backward the same way (do[t][h][d] = sum_j dy[t][j] wo[j][h*D+d],
+    dwo[j][h*D+d] = sum_t dy[t][j] o[t][h][d])."""
+    r = _rng(31)
+    T, H, D, hidden = 5, 3, 2, 4
+    o, wo, dy = r.standard_normal((T, H, D)), r.standard_normal((hidden, H * D)), \
+        r.standard_normal((T, hidden))
+    y = O.output_projection(o, wo)
+    do, dwo = O.output_projection_backward(o, wo, dy)
+    for t in range(T):
+        for j in range(hidden):
+            ref = sum(o[t, h, d] * wo[j, h * D + d] for h in range(H) for d in range(D))
+            assert abs(y[t, j] - ref) < 1e-12
+    for t in range(T):
+        for h in range(H):
+            for d in range(D):
+                ref = sum(dy[t, j] * wo[j, h * D + d] for j in range(hidden))
+                assert abs(do[t, h * D + d] - ref) < 1e-12
+    for j in range(hidden):
+        for h in range(H):
+            for d in range(D):
+                ref = sum(dy[t, j] * o[t, h, d] for t in range(T))
+                assert abs(dwo[j, h * D + d] - ref) < 1e-12
+
+
+def test_layer_sharded_output_projection_equals_unsharded():
+    """Per-rank projection of the restored shards equals one projection of the whole
+    sequence, and head->seq followed by it equals summing each rank's head group of the
+    head layout (the arithmetic is the same, only the order of the data differs)."""
+    S, hidden, H, G, D, P = 16, 8, 4, 2, 4, 2
+    r = _rng(32)
+    x, w = r.standard_normal((S, hidden)), 0.3 * r.standard_normal(((H + 2 * G) * D, hidden))
+    wo = r.standard_normal((hidden, H * D))
+    y, _, o_seq = O.ulysses_layer_forward(x, w, wo, P, H, G, D)
+    assert np.allclose(y, O.output_projection(o_seq.reshape(S, H, D), wo), rtol=0, atol=1e-12)
+    _, _, (_, _, _, _, o_head) = O.ulysses_block_forward(x, w, P, H, G, D)
+    hp = H // P
+    y2 = sum(o_head[r2].reshape(S, hp * D) @ wo[:, r2 * hp * D:(r2 + 1) * hp * D].T
+             for r2 in range(P))
+    assert np.allclose(y, y2, rtol=0, atol=1e-12)
+
+
+def test_layer_backward_matches_torch_autograd():
+    """Whole block with the output projection: dx, dw, dwo and dO against torch float64
+    autograd of an independent torch restatement."""
+    S, hidden, H, G, D, P, theta = 32, 16, 4, 2, 8, 2, 10000.0
+    r = _rng(33)
+    x, w = r.standard_normal((S, hidden)), 0.3 * r.standard_normal(((H + 2 * G) * D, hidden))
+    wo = 0.3 * r.standard_normal((hidden, H * D))
+    dy = r.standard_normal((S, hidden))
+    dx, dw, dwo, do_seq = O.ulysses_layer_backward(x, w, wo, dy, P, H, G, D, theta)
+    tx, tw, two = (torch.from_numpy(a).clone().requires_grad_(True) for a in (x, w, wo))
+    y = (tx @ tw.T).reshape(S, H + 2 * G, D)
+    half = D // 2
+    phi = torch.from_numpy(O.rope_angles(np.arange(S), D, theta))[:, None, :]
+
+    def rope(t):
+        lo, hi = t[..., :half], t[..., half:]
+        return torch.cat([lo * torch.cos(phi) - hi * torch.sin(phi),
+                          hi * torch.cos(phi) + lo * torch.sin(phi)], -1)
+
+    q, k, v = rope(y[:, :H]), rope(y[:, H:H + G]), y[:, H + G:]
+    o = _torch_attention(q, k, v, H, G)
+    o.retain_grad()
+    out = o.reshape(S, H * D) @ two.T
+    (out * torch.from_numpy(dy)).sum().backward()
+    assert np.allclose(dx, tx.grad.numpy(), rtol=0, atol=1e-10)
+    assert np.allclose(dw, tw.grad.numpy(), rtol=0, atol=1e-10)
+    assert np.allclose(dwo, two.grad.numpy(), rtol=0, atol=1e-10)
+    assert np.allclose(do_seq, o.grad.numpy().reshape(S, H, D), rtol=0, atol=1e-10)
