@@ -184,6 +184,24 @@ uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void *dq, const void *dk
 uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void *x, const void *w,
                                 const void *dqkv, void *dx, float *dw, void *stream);
 
+/* Output projection of the block, fused with the head->seq all-to-all of O ("Snowflake's
+ * Ulysses trick ...", para 2: the inverse all-to-all restores the sequence sharding, after
+ * which the block's output projection runs on each rank's tokens):
+ *   y[s][j] = sum_{h,d} o_seq[s][h][d] * wo[j][h*D + d]
+ * read straight from the attention's head layout o_head [P][S][H/P][D] (bf16), so O is never
+ * stored in the sequence layout.  wo: bf16 [hidden][H*D] (nn.Linear layout).  y: bf16
+ * [S][hidden] (= [P][S/P][hidden]), fp32 accumulation, round to nearest even. */
+uly_status ulysses_o_proj(uly_plan plan, const void *o_head, const void *wo, void *y,
+                          void *stream);
+
+/* Backward of ulysses_o_proj, fused with the seq->head all-to-all of dO:
+ *   do_head (bf16, head layout [P][S][H/P][D]) = dy wo, written straight in the layout
+ *     ulysses_attn_bwd reads;
+ *   dwo (fp32 [hidden][H*D]) = dy^T o_seq, summed over all S tokens of all shards.
+ * dy: bf16 [S][hidden].  Either output may be NULL to skip it. */
+uly_status ulysses_o_proj_bwd(uly_plan plan, const void *o_head, const void *wo,
+                              const void *dy, void *do_head, float *dwo, void *stream);
+
 /* Synchronises `stream`, reads the plan's device status word, clears it and returns it
  * (ULY_OK, or e.g. ULY_ERR_TIMEOUT).  ULY_ERR_CUDA if the synchronisation itself fails. */
 uly_status ulysses_sync_status(uly_plan plan, void *stream);

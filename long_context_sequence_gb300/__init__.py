@@ -23,6 +23,7 @@ EXPORTED = ("ulysses_plan", "ulysses_plan_destroy", "ulysses_workspace_bytes",
             "ulysses_qkv_proj", "ulysses_seq_to_head", "ulysses_seq_to_head_heads",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc",
             "ulysses_head_to_seq", "ulysses_head_to_seq_qkv", "ulysses_qkv_proj_bwd",
+            "ulysses_o_proj", "ulysses_o_proj_bwd",
             "ulysses_sync_status", "ulysses_bytes_moved", "ulysses_a2a_volume",
             "ulysses_last_error")
 
@@ -77,6 +78,8 @@ def load_library(path: str = LIB_PATH):
         "ulysses_head_to_seq": ([vp, vp, i32, vp, vp], i32),
         "ulysses_head_to_seq_qkv": ([vp, vp, vp, vp, i32, vp, vp], i32),
         "ulysses_qkv_proj_bwd": ([vp] * 7, i32),
+        "ulysses_o_proj": ([vp] * 5, i32),
+        "ulysses_o_proj_bwd": ([vp] * 7, i32),
         "ulysses_sync_status": ([vp, vp], i32),
         "ulysses_bytes_moved": ([vp], u64),
         "ulysses_a2a_volume": ([ctypes.POINTER(UlyConfig), ctypes.POINTER(u64),
@@ -213,6 +216,16 @@ def ulysses_head_to_seq_qkv(plan, dq, dk, dv, dqkv_seq, apply_rope=False, stream
 def ulysses_qkv_proj_bwd(plan, x, w, dqkv, dx=None, dw=None, stream=None):
     _check(load_library().ulysses_qkv_proj_bwd(plan.handle, _ptr(x), _ptr(w), _ptr(dqkv),
                                                _ptr(dx), _ptr(dw), _stream(stream)))
+
+
+def ulysses_o_proj(plan, o_head, wo, y, stream=None):
+    _check(load_library().ulysses_o_proj(plan.handle, _ptr(o_head), _ptr(wo), _ptr(y),
+                                         _stream(stream)))
+
+
+def ulysses_o_proj_bwd(plan, o_head, wo, dy, do_head=None, dwo=None, stream=None):
+    _check(load_library().ulysses_o_proj_bwd(plan.handle, _ptr(o_head), _ptr(wo), _ptr(dy),
+                                             _ptr(do_head), _ptr(dwo), _stream(stream)))
 
 
 def ulysses_sync_status(plan, stream=None) -> int:

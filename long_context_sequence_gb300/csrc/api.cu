@@ -84,6 +84,25 @@ bool make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_
   return true;
 }
 
+bool make_tmap_3d_bf16(CUtensorMap* m, const void* base, const uint64_t dims_in[3],
+                       const uint64_t strides_bytes[2], uint32_t box0, uint32_t box1,
+                       const char** err) {
+  EncodeTiledFn fn = encode_fn(err);
+  if (!fn) return false;
+  cuuint64_t dims[3] = {dims_in[0], dims_in[1], dims_in[2]};
+  cuuint64_t strides[2] = {strides_bytes[0], strides_bytes[1]};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (err) *err = "cuTensorMapEncodeTiled (3-D) rejected the layout";
+    return false;
+  }
+  return true;
+}
+
 bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims_in[4],
                        const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
                        const char** err) {
@@ -383,6 +402,32 @@ uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void* x, const void* w, con
   if (p.S > (int64_t(1) << 31) - 1) return fail(ULY_ERR_UNSUPPORTED, "S too large");
   return launched(uly::launch_qkv_gemm_bwd(p, x, w, dqkv, dx, dw, as_stream(stream)),
                   "qkv_proj_bwd launch");
+}
+
+uly_status ulysses_o_proj(uly_plan plan, const void* o_head, const void* wo, void* y,
+                          void* stream) {
+  if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  const Plan& p = plan->p;
+  if (p.S == 0) return ULY_OK;
+  if (!o_head || !wo || !y) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(o_head) || !aligned16(wo) || !aligned16(y))
+    return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (p.S > (int64_t(1) << 31) - 1) return fail(ULY_ERR_UNSUPPORTED, "S too large");
+  return launched(uly::launch_o_proj(p, o_head, wo, y, as_stream(stream)), "o_proj launch");
+}
+
+uly_status ulysses_o_proj_bwd(uly_plan plan, const void* o_head, const void* wo, const void* dy,
+                              void* do_head, float* dwo, void* stream) {
+  if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  const Plan& p = plan->p;
+  if (p.S == 0) return ULY_OK;
+  if (!o_head || !wo || !dy) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(o_head) || !aligned16(wo) || !aligned16(dy) || !aligned16(do_head) ||
+      !aligned16(dwo))
+    return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (p.S > (int64_t(1) << 31) - 1) return fail(ULY_ERR_UNSUPPORTED, "S too large");
+  return launched(uly::launch_o_proj_bwd(p, o_head, wo, dy, do_head, dwo, as_stream(stream)),
+                  "o_proj_bwd launch");
 }
 
 uly_status ulysses_sync_status(uly_plan plan, void* stream) {

@@ -42,6 +42,10 @@ cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk
 cudaError_t launch_qkv_gemm(const Plan& p, const void* x, const void* w, void* out,
                             cudaStream_t st);
 // dx = dqkv w (bf16 [S][hidden]) and dw = dqkv^T x (fp32 [C][hidden]); either may be null.
+cudaError_t launch_o_proj(const Plan& p, const void* o_head, const void* wo, void* y,
+                          cudaStream_t st);
+cudaError_t launch_o_proj_bwd(const Plan& p, const void* o_head, const void* wo, const void* dy,
+                              void* do_head, float* dwo, cudaStream_t st);
 cudaError_t launch_qkv_gemm_bwd(const Plan& p, const void* x, const void* w, const void* dqkv,
                                 void* dx, float* dw, cudaStream_t st);
 cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v,
@@ -63,6 +67,11 @@ size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off)
 // Returns false and sets *err on failure.
 bool make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                       const char** err);
+// 3-D bf16 map over [parts][rows][x] with byte strides {row, part} and a box of
+// {box0, box1, 1}; 128-byte swizzle, out-of-range elements read as zero.
+bool make_tmap_3d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[3],
+                       const uint64_t strides_bytes[2], uint32_t box0, uint32_t box1,
                        const char** err);
 // 4-D bf16 map over [d3][d2][d1][d0] (d0 innermost) with byte strides s1, s2, s3 and a box
 // of {box0, 1, box2, 1}; 128-byte swizzle, out-of-range elements read as zero.

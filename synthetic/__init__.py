@@ -26,6 +26,7 @@ _SO = os.path.join(_HERE, "libsynth.so")
 _lib = None
 
 TENSOR_X, TENSOR_W, TENSOR_Q, TENSOR_K, TENSOR_V, TENSOR_QKV = 0, 1, 2, 3, 4, 5
+TENSOR_WO = 6          # output projection weight (seed 0); with seed 1, the gradient dy
 SEED_FWD, SEED_DO, SEED_SAMPLE = 0, 1, 2
 
 
