@@ -224,24 +224,27 @@ def run_ours(args):
              "attn_bwd", "head_to_seq_grads"]
     launches_per_step = 1 + 1 + 1 + 1 + 1 + 3 + 1
 
-    def step(ev=None):
+    def step(ev=None, io=None):
+        # io: the step's input and output buffers (x, dO_seq, o_seq, dqkv_seq)
+        xs, dos, os_, dqs = io if io is not None else (x, do_seq, o_seq, dqkv_seq)
+
         def mark(i):
             if ev is not None:
                 ev[i].record(stream)
         mark(0)
-        U.ulysses_qkv_proj(plan, x, wq, qkv, sid)
+        U.ulysses_qkv_proj(plan, xs, wq, qkv, sid)
         mark(1)
         U.ulysses_seq_to_head(plan, qkv, q, k, v, apply_rope=True, stream=sid)
         mark(2)
         U.ulysses_attn_fwd(plan, q, k, v, o, lse, sid, o_lo=o_lo)
         mark(3)
-        U.ulysses_head_to_seq(plan, o, H, o_seq, sid)
+        U.ulysses_head_to_seq(plan, o, H, os_, sid)
         mark(4)
-        U.ulysses_seq_to_head_heads(plan, do_seq, H, do, sid)
+        U.ulysses_seq_to_head_heads(plan, dos, H, do, sid)
         mark(5)
         U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid, o_lo=o_lo)
         mark(6)
-        U.ulysses_head_to_seq_qkv(plan, dq, dk, dv, dqkv_seq, apply_rope=True, stream=sid)
+        U.ulysses_head_to_seq_qkv(plan, dq, dk, dv, dqs, apply_rope=True, stream=sid)
         mark(7)
 
     for _ in range(args.warmup):
@@ -291,66 +294,135 @@ def run_ours(args):
     qkv_tflops = 2.0 * S * hidden * C / (avg["qkv_proj"] * 1e-3) / 1e12
     s2h_gbs = perm_bytes["seq_to_head"] / (avg["seq_to_head"] * 1e-3) / 1e9
 
-    # end to end through the same calls, with the step's inputs coming from pinned host
-    # memory and its outputs read back, copies inside the timed region
+    # End to end through the same calls: every step copies its inputs (x, dO) from pinned
+    # host memory and reads its outputs (o_seq, dqkv_seq) back, all inside the timed region.
+    # The copies run on two copy streams (up, down) with two buffer sets, so step i's read-back and
+    # step i+1's upload overlap the compute of the steps next to them, as a training loop
+    # that streams its activations would run.
     e2e = None
     if not args.no_e2e:
         hx = torch.empty(sh["x"], dtype=bf, pin_memory=True)
         hdo = torch.empty(sh["o_seq"], dtype=bf, pin_memory=True)
         hx.copy_(x)
         hdo.copy_(do_seq)
-        outs = [o_seq, dqkv_seq]
-        houts = [torch.empty(t.shape, dtype=bf, pin_memory=True) for t in outs]
+        sets = [(x, do_seq, o_seq, dqkv_seq),
+                (torch.empty_like(x), torch.empty_like(do_seq), torch.empty_like(o_seq),
+                 torch.empty_like(dqkv_seq))]
+        houts = [[torch.empty(t.shape, dtype=bf, pin_memory=True) for t in (o_seq, dqkv_seq)]
+                 for _ in range(2)]
         h2d = hx.numel() * 2 + hdo.numel() * 2
-        d2h = sum(t.numel() * 2 for t in outs)
+        d2h = o_seq.numel() * 2 + dqkv_seq.numel() * 2
+        up = torch.cuda.Stream(dev)      # host -> device
+        down = torch.cuda.Stream(dev)    # device -> host
+        ev = lambda: torch.cuda.Event()   # noqa: E731
+        uploaded = [ev(), ev()]     # inputs of set b are on the device
+        computed = [ev(), ev()]     # the step on set b is done (inputs free, outputs ready)
+        read_back = [ev(), ev()]    # outputs of set b are on the host
 
-        def e2e_step():
-            x.copy_(hx, non_blocking=True)
-            do_seq.copy_(hdo, non_blocking=True)
-            step()
-            for h_, d_ in zip(houts, outs):
-                h_.copy_(d_, non_blocking=True)
+        def e2e_run(n):
+            for i in range(n):
+                b = i % 2
+                xs, dos, os_, dqs = sets[b]
+                with torch.cuda.stream(up):
+                    if i >= 2:
+                        up.wait_event(computed[b])
+                    xs.copy_(hx, non_blocking=True)
+                    dos.copy_(hdo, non_blocking=True)
+                    uploaded[b].record(up)
+                stream.wait_event(uploaded[b])
+                if i >= 2:
+                    stream.wait_event(read_back[b])
+                step(io=sets[b])
+                computed[b].record(stream)
+                with torch.cuda.stream(down):
+                    down.wait_event(computed[b])
+                    houts[b][0].copy_(os_, non_blocking=True)
+                    houts[b][1].copy_(dqs, non_blocking=True)
+                    read_back[b].record(down)
+            for b in range(min(n, 2)):
+                stream.wait_event(read_back[b])
 
-        e2e_step()
+        e2e_run(2)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
+        torch.cuda.synchronize()
         e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
+        up.wait_event(e0)
+        down.wait_event(e0)
+        e2e_run(args.steps)
         e1.record(stream)
         torch.cuda.synchronize()
         ems = reduce_max_ms(e0.elapsed_time(e1) / args.steps, world, dist, dev)
+        # the last step's outputs arrived on the host intact
+        last = (args.steps - 1) % 2
+        if not (torch.equal(houts[last][0], sets[last][2].cpu()) and
+                torch.equal(houts[last][1], sets[last][3].cpu())):
+            raise RuntimeError("e2e read-back differs from the device result")
         e2e = {"value": job_tflops(fwd_f + bwd_f, world, ems), "unit": "TFLOPS",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ems,
+               "copies": "H2D and D2H streams, double-buffered, overlapped with compute"}
 
-    # rest of the block's training step, timed on its own: the QKV projection backward
-    # (dx = dqkv w, dw = dqkv^T x) on the gradient the step just produced
-    pbwd = None
-    if not args.no_proj_bwd:
+    # The whole attention layer's training step, timed on its own after the hot-path step:
+    # projection, seq->head (RoPE), attention forward, output projection read straight from
+    # the head layout, its backward written straight into the head layout, attention
+    # backward, gradient head->seq (RoPE backward), projection backward.
+    layer = None
+    if not args.no_layer:
+        wo = (torch.randn((hidden, H * D), generator=gen, device=dev) * 0.02).to(bf)
+        dy = torch.randn((S, hidden), generator=gen, device=dev).to(bf)
+        y = torch.empty((S, hidden), dtype=bf, device=dev)
         dx = torch.empty(sh["x"], dtype=bf, device=dev)
         dw = torch.empty(sh["w"], dtype=torch.float32, device=dev)
-        for _ in range(args.warmup):
+        dwo = torch.empty((hidden, H * D), dtype=torch.float32, device=dev)
+        lnames = ["qkv_proj", "seq_to_head", "attn_fwd", "o_proj", "o_proj_bwd", "attn_bwd",
+                  "head_to_seq_grads", "qkv_proj_bwd"]
+
+        def layer_step(ev=None):
+            def mark(i):
+                if ev is not None:
+                    ev[i].record(stream)
+            mark(0)
+            U.ulysses_qkv_proj(plan, x, wq, qkv, sid)
+            mark(1)
+            U.ulysses_seq_to_head(plan, qkv, q, k, v, apply_rope=True, stream=sid)
+            mark(2)
+            U.ulysses_attn_fwd(plan, q, k, v, o, lse, sid, o_lo=o_lo)
+            mark(3)
+            U.ulysses_o_proj(plan, o, wo, y, sid)
+            mark(4)
+            U.ulysses_o_proj_bwd(plan, o, wo, dy, do, dwo, sid)
+            mark(5)
+            U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid, o_lo=o_lo)
+            mark(6)
+            U.ulysses_head_to_seq_qkv(plan, dq, dk, dv, dqkv_seq, apply_rope=True, stream=sid)
+            mark(7)
             U.ulysses_qkv_proj_bwd(plan, x, wq, dqkv_seq, dx, dw, sid)
-        pev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+            mark(8)
+
+        for _ in range(args.warmup):
+            layer_step()
+        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
         torch.cuda.synchronize()
-        for e in pev:
-            e[0].record(stream)
-            U.ulysses_qkv_proj_bwd(plan, x, wq, dqkv_seq, dx, None, sid)
-            e[1].record(stream)
-            U.ulysses_qkv_proj_bwd(plan, x, wq, dqkv_seq, None, dw, sid)
-            e[2].record(stream)
+        for e in lev:
+            layer_step(e)
         torch.cuda.synchronize()
         st = U.ulysses_sync_status(plan, sid)
         if st != U.ULY_OK:
             raise RuntimeError("device status %d: %s" % (st, U.ulysses_last_error()))
-        dx_ms = sum(e[0].elapsed_time(e[1]) for e in pev) / len(pev)
-        dw_ms = sum(e[1].elapsed_time(e[2]) for e in pev) / len(pev)
-        gf = 2.0 * S * hidden * C
-        pbwd = {"dx_ms": dx_ms, "dw_ms": dw_ms, "dx_tflops": gf / (dx_ms * 1e-3) / 1e12,
-                "dw_tflops": gf / (dw_ms * 1e-3) / 1e12,
-                "block_train_step_ms": ms_step + dx_ms + dw_ms}
+        lper = {n: sum(e[i].elapsed_time(e[i + 1]) for e in lev) / len(lev)
+                for i, n in enumerate(lnames)}
+        lms = sum(e[0].elapsed_time(e[8]) for e in lev) / len(lev)
+        proj_f = 2.0 * S * hidden * C          # each of the three QKV GEMMs
+        oproj_f = 2.0 * S * hidden * H * D     # each of the three output-projection GEMMs
+        layer_f = fwd_f + bwd_f + 3 * proj_f + 3 * oproj_f
+        layer = {"ms_per_step": lms, "tflops": layer_f / (lms * 1e-3) / 1e12,
+                 "flops_per_step": layer_f, "kernels_ms": lper,
+                 "o_proj_tflops": oproj_f / (lper["o_proj"] * 1e-3) / 1e12,
+                 "o_proj_bwd_tflops": 2 * oproj_f / (lper["o_proj_bwd"] * 1e-3) / 1e12,
+                 "qkv_proj_bwd_tflops": 2 * proj_f / (lper["qkv_proj_bwd"] * 1e-3) / 1e12,
+                 "launches_per_step": 1 + 1 + 1 + 1 + 2 + 3 + 1 + 2}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -380,7 +452,7 @@ def run_ours(args):
             "seq_to_head_gbs": s2h_gbs, "peaks": peaks, "peaks_source": peak_kind,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
-            "qkv_proj_bwd": pbwd,
+            "layer_train_step": layer,
         }
         print(json.dumps(line))
     plan.close()
@@ -396,7 +468,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seq", type=int, default=0, help="override S (quick checks only)")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-proj-bwd", action="store_true")
+    ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.seq:

@@ -276,11 +276,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&qd_empty[st]);
         return true;
       };
+      // Items are issued in pairs, one per region: MMA2 of both, then MMA1 of the next
+      // two.  MMA1(it+2) waits for region X's dQ^T read-out; by then the other region's
+      // MMA2 already sits in the tensor pipe, so that latency is hidden behind it.
       bool alive = mbar_wait(kv_full, 0, wc);
       for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma1(it);
-      for (int it = 0; alive && it < n_items; ++it) {
+      for (int it = 0; alive && it < n_items; it += 2) {
         alive = mma2(it);
+        if (alive && it + 1 < n_items) alive = mma2(it + 1);
         if (alive && it + 2 < n_items) alive = mma1(it + 2);
+        if (alive && it + 3 < n_items) alive = mma1(it + 3);
       }
       if (alive) mma_commit(acc_done);
       mma_commit(drain);
