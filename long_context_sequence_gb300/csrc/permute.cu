@@ -7,6 +7,8 @@
 // Contexts", para 5).  The kernels move 16-byte vectors; for every token the source row
 // is contiguous and the destination runs are (heads per rank) * D * 2 bytes long, so both
 // sides stay coalesced.  The memory-bound roofline is read + write bytes / HBM bandwidth.
+// The q/k/v kernels, which may apply RoPE, give each thread one 8-pair chunk of one token
+// across all its heads, so the token's angles are built once, not once per head.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -65,29 +67,64 @@ __device__ __forceinline__ void load8(const void* row, int elem, float (&f)[8], 
   }
 }
 
+// RoPE angles of one token for the 8 pairs (e, e + D/2), e = e0 .. e0 + 7: (cos, sin) of
+// s * theta^(-2e/D), rebuilt from the two-level table by angle addition (hi: multiples of
+// kRopeL positions, lo: the remainder).  The angles depend on the token and the pair only,
+// so a thread computes them once and applies them to every rotated head of its token.
+__device__ __forceinline__ void rope_angles8(const RopeTab& rope, int64_t s, int e0,
+                                             float (&cs)[8], float (&sn)[8]) {
+  const int64_t sh = s / kRopeL;
+  const int sl = (int)(s - sh * kRopeL);
+  const float2* th = rope.hi + sh * rope.half + e0;
+  const float2* tl = rope.lo + (int64_t)sl * rope.half + e0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 a = __ldg(th + i), b = __ldg(tl + i);
+    cs[i] = fmaf(a.x, b.x, -a.y * b.y);
+    sn[i] = fmaf(a.y, b.x, a.x * b.y);
+  }
+}
+
+// Thread <-> (token, chunk): a block covers kThreads / (D/16) tokens; a thread owns the
+// elements [8u, 8u+8) and their RoPE partners [D/2 + 8u, D/2 + 8u + 8) of every head row of
+// its token.  Per head it moves 2 x 16 bytes in and out (a warp: 4 tokens x 128-byte runs
+// at D = 128).
+struct TokenChunk {
+  int64_t s;
+  int cu;
+  bool valid;
+};
+__device__ __forceinline__ TokenChunk token_chunk(int64_t b, int upr, int64_t S) {
+  const int tpb = kThreads / upr;
+  const int t = threadIdx.x / upr;
+  TokenChunk r;
+  r.s = b * tpb + t;
+  r.cu = threadIdx.x - t * upr;
+  r.valid = t < tpb && r.s < S;
+  return r;
+}
+
 // seq->head with the q/k/v split, optional fp32 input and optional RoPE on q and k.
-// Work unit = one token's head row, elements [8u, 8u+8) and their RoPE partners
-// [D/2 + 8u, D/2 + 8u + 8).
 template <bool kFp32In, bool kRope>
 __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
     const void* __restrict__ in, __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
     __nv_bfloat16* __restrict__ v, int64_t S, int P, int H, int G, int D, RopeTab rope) {
   const int C = H + 2 * G;
-  const int upr = D / 16;              // units per head row
-  const int U = C * upr;               // units per token
+  const int upr = D / 16;
   const int hq = H / P, hk = G / P;
-  const int64_t n_blocks = (S + kTokensPerBlock - 1) / kTokensPerBlock;
+  const int64_t n_blocks = (S + kThreads / upr - 1) / (kThreads / upr);
   const size_t esz = kFp32In ? 4 : 2;
   for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
-    const int64_t s0 = b * kTokensPerBlock;
-    const int ntok = (int)(S - s0 < kTokensPerBlock ? S - s0 : kTokensPerBlock);
-    for (int w = threadIdx.x; w < ntok * U; w += kThreads) {
-      const int tl = w / U;
-      const int unit = w - tl * U;
-      const int c = unit / upr;
-      const int cu = unit - c * upr;
-      const int64_t s = s0 + tl;
-      const char* src = reinterpret_cast<const char*>(in) + ((size_t)s * C + c) * D * esz;
+    const TokenChunk tc = token_chunk(b, upr, S);
+    if (!tc.valid) continue;
+    const int64_t s = tc.s;
+    const int e_lo = tc.cu * 8, e_hi = D / 2 + tc.cu * 8;
+    float cs[8], sn[8];
+    if (kRope) rope_angles8(rope, s, e_lo, cs, sn);
+    const char* row = reinterpret_cast<const char*>(in) + (size_t)s * C * D * esz;
+#pragma unroll 2
+    for (int c = 0; c < C; ++c) {
+      const char* src = row + (size_t)c * D * esz;
       __nv_bfloat16* dst;
       if (c < H) {
         const int r2 = c / hq, hh = c - r2 * hq;
@@ -99,24 +136,16 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
         const int g = c - H - G, r2 = g / hk, hh = g - r2 * hk;
         dst = v + (((size_t)r2 * S + s) * hk + hh) * D;
       }
-      const int e_lo = cu * 8, e_hi = D / 2 + cu * 8;
       float lo[8], hi[8];
       uint4 raw_lo, raw_hi;
       load8<kFp32In>(src, e_lo, lo, raw_lo);
       load8<kFp32In>(src, e_hi, hi, raw_hi);
       if (kRope && c < H + G) {
-        const int64_t sh = s / kRopeL;
-        const int sl = (int)(s - sh * kRopeL);
-        const float2* th = rope.hi + sh * rope.half + e_lo;
-        const float2* tl2 = rope.lo + (int64_t)sl * rope.half + e_lo;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 a = __ldg(th + i), bb = __ldg(tl2 + i);
-          const float cs = fmaf(a.x, bb.x, -a.y * bb.y);
-          const float sn = fmaf(a.y, bb.x, a.x * bb.y);
           const float x0 = lo[i], x1 = hi[i];
-          lo[i] = fmaf(x0, cs, -x1 * sn);
-          hi[i] = fmaf(x1, cs, x0 * sn);
+          lo[i] = fmaf(x0, cs[i], -x1 * sn[i]);
+          hi[i] = fmaf(x1, cs[i], x0 * sn[i]);
         }
         st_stream(dst + e_lo, pack8(lo));
         st_stream(dst + e_hi, pack8(hi));
@@ -133,7 +162,7 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
 
 // Inverse of seq_to_head for the gradients: dq [P][S][H/P][D], dk, dv [P][S][G/P][D] ->
 // dqkv [S][H + 2G][D], with the RoPE backward on the q and k parts (each pair turned back
-// by its angle: lo' = lo cos + hi sin, hi' = hi cos - lo sin).  Same work units as above.
+// by its angle: lo' = lo cos + hi sin, hi' = hi cos - lo sin).  Same thread mapping.
 template <bool kRope>
 __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
     const __nv_bfloat16* __restrict__ dq, const __nv_bfloat16* __restrict__ dk,
@@ -141,18 +170,18 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
     int H, int G, int D, RopeTab rope) {
   const int C = H + 2 * G;
   const int upr = D / 16;
-  const int U = C * upr;
   const int hq = H / P, hk = G / P;
-  const int64_t n_blocks = (S + kTokensPerBlock - 1) / kTokensPerBlock;
+  const int64_t n_blocks = (S + kThreads / upr - 1) / (kThreads / upr);
   for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
-    const int64_t s0 = b * kTokensPerBlock;
-    const int ntok = (int)(S - s0 < kTokensPerBlock ? S - s0 : kTokensPerBlock);
-    for (int w = threadIdx.x; w < ntok * U; w += kThreads) {
-      const int tl = w / U;
-      const int unit = w - tl * U;
-      const int c = unit / upr;
-      const int cu = unit - c * upr;
-      const int64_t s = s0 + tl;
+    const TokenChunk tc = token_chunk(b, upr, S);
+    if (!tc.valid) continue;
+    const int64_t s = tc.s;
+    const int e_lo = tc.cu * 8, e_hi = D / 2 + tc.cu * 8;
+    float cs[8], sn[8];
+    if (kRope) rope_angles8(rope, s, e_lo, cs, sn);
+    __nv_bfloat16* row = out + (size_t)s * C * D;
+#pragma unroll 2
+    for (int c = 0; c < C; ++c) {
       const __nv_bfloat16* src;
       if (c < H) {
         const int r2 = c / hq, hh = c - r2 * hq;
@@ -164,25 +193,17 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
         const int g = c - H - G, r2 = g / hk, hh = g - r2 * hk;
         src = dv + (((size_t)r2 * S + s) * hk + hh) * D;
       }
-      __nv_bfloat16* dst = out + ((size_t)s * C + c) * D;
-      const int e_lo = cu * 8, e_hi = D / 2 + cu * 8;
+      __nv_bfloat16* dst = row + (size_t)c * D;
       const uint4 raw_lo = ld_stream(src + e_lo), raw_hi = ld_stream(src + e_hi);
       if (kRope && c < H + G) {
         float lo[8], hi[8];
         unpack8(raw_lo, lo);
         unpack8(raw_hi, hi);
-        const int64_t sh = s / kRopeL;
-        const int sl = (int)(s - sh * kRopeL);
-        const float2* th = rope.hi + sh * rope.half + e_lo;
-        const float2* tl2 = rope.lo + (int64_t)sl * rope.half + e_lo;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float2 a = __ldg(th + i), bb = __ldg(tl2 + i);
-          const float cs = fmaf(a.x, bb.x, -a.y * bb.y);
-          const float sn = fmaf(a.y, bb.x, a.x * bb.y);
           const float x0 = lo[i], x1 = hi[i];
-          lo[i] = fmaf(x0, cs, x1 * sn);
-          hi[i] = fmaf(x1, cs, -x0 * sn);
+          lo[i] = fmaf(x0, cs[i], x1 * sn[i]);
+          hi[i] = fmaf(x1, cs[i], -x0 * sn[i]);
         }
         st_stream(dst + e_lo, pack8(lo));
         st_stream(dst + e_hi, pack8(hi));
@@ -231,11 +252,19 @@ int permute_grid(const Plan& p, int64_t S) {
   return (int)(blocks < cap ? blocks : cap);
 }
 
+// Grid of the token-chunk kernels (kThreads / (D/16) tokens per block).
+int token_chunk_grid(const Plan& p, int64_t S) {
+  const int64_t tpb = kThreads / (p.D / 16);
+  const int64_t blocks = (S + tpb - 1) / tpb;
+  const int64_t cap = (int64_t)num_sms(p.device) * 8;
+  return (int)(blocks < cap ? blocks : cap);
+}
+
 }  // namespace
 
 cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool rope, void* q,
                                void* k, void* v, cudaStream_t st) {
-  const int grid = permute_grid(p, p.S);
+  const int grid = token_chunk_grid(p, p.S);
   RopeTab tab{p.rope_hi, p.rope_lo, p.D / 2};
   auto* qb = static_cast<__nv_bfloat16*>(q);
   auto* kb = static_cast<__nv_bfloat16*>(k);
@@ -253,7 +282,7 @@ cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool
 
 cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk,
                                    const void* dv, bool rope, void* out, cudaStream_t st) {
-  const int grid = permute_grid(p, p.S);
+  const int grid = token_chunk_grid(p, p.S);
   RopeTab tab{p.rope_hi, p.rope_lo, p.D / 2};
   auto* a = static_cast<const __nv_bfloat16*>(dq);
   auto* b = static_cast<const __nv_bfloat16*>(dk);
