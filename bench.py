@@ -39,6 +39,27 @@ def attn_flops(S, H, D):
     return fwd, 2.5 * fwd
 
 
+# DRAM bytes of one ulysses_attn_bwd call at the bench workload (S=131072), summed over its
+# kernels (bwd_pre, 2 x to_f16, attn_bwd_kernel, bwd_dq), from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none).
+# Valid only for the kernel source it was taken on: the figure is dropped (null) as soon as
+# the hash of that source changes.
+BWD_TRAFFIC = {"bytes": (4.30 + 4.26 + 2 * (0.26848 + 0.21543) + 17.35 + 8.85 + 2.15 + 1.04) * 1e9,
+               "seq_len": 131072,
+               "source_sha256": "4acd565449134d18669ff5cab2a3b5f305db33d5ddf62721a90a56fc9d87d410"}
+
+
+def bwd_traffic(seq_len):
+    import hashlib
+    h = hashlib.sha256()
+    for f in ("attn_bwd.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "long_context_sequence_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    if h.hexdigest() != BWD_TRAFFIC["source_sha256"] or seq_len != BWD_TRAFFIC["seq_len"]:
+        return None
+    return BWD_TRAFFIC["bytes"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -443,7 +464,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (no flush)"},
             "roofline": {"kernel": "ulysses_attn_bwd", "bound": "tensor",
                          "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": bwd_tflops / peak, "traffic": None,
+                         "frac": bwd_tflops / peak, "traffic": bwd_traffic(S),
                          "peak_source": "%s bf16_tflops_sustained" % peak_kind},
             "kernels_ms": avg,
             "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
