@@ -35,8 +35,8 @@ Points the pages leave open are read as follows (the plainest reading):
 Pins (tests/test_oracle.py): brute-force loops on tiny inputs, a hand-worked attention
 example and a hand-written all-to-all index table under tests/golden/, closed forms
 (Q = 0 gives prefix means and lse = ln(i+1)), invariants (round trip, sharded equals
-unsharded, norm-preserving RoPE, softmax shift invariance, sum of dK is zero), torch
-float64 SDPA and autograd, and central finite differences.
+unsharded, norm-preserving RoPE, softmax shift invariance, sum of dK is zero, ring attention
+equals unsharded attention), torch float64 SDPA and autograd, and central finite differences.
 """
 from __future__ import annotations
 
@@ -391,3 +391,63 @@ def ulysses_layer_backward(x, w, wo, dy, P: int, H: int, G: int, D: int, theta: 
     do_seq, dwo = output_projection_backward(o_seq.reshape(S, H, D), wo, dy)
     dx, dw, _ = ulysses_block_backward(x, w, do_seq, P, H, G, D, theta, scale)
     return dx, dw, dwo, do_seq.reshape(S, H, D)
+
+
+# --------------------------------------------------------------- ring attention (comparator)
+# The pages set Ulysses against ring attention, whose per-GPU communication is O(hidden * S)
+# against Ulysses' O(hidden * S / P) [UT para 3].  Ring attention keeps the sequence sharding
+# throughout: rank r holds its queries and, in step t = 0 .. P-1, the K/V shard
+# (r - t) mod P; after each step every rank passes the shard it holds to rank r + 1.
+def ring_attention(q_seq, k_seq, v_seq, scale=None):
+    """Ring attention on P ranks, causal by global token position, GQA.
+
+    q_seq [P][S/P][H][D]; k_seq, v_seq [P][S/P][G][D] (rank r starts with shard r).  Each
+    rank keeps a running row max m, sum l and accumulator acc over the shards it has seen
+    (rows of a step with no visible key leave the state unchanged) and divides by l at the
+    end.  Returns o_seq [P][S/P][H][D], lse [P][H][S/P] and the bytes each rank sent
+    (it forwards its K/V shard P - 1 times, bf16)."""
+    q = np.asarray(q_seq, np.float64)
+    k = np.asarray(k_seq, np.float64)
+    v = np.asarray(v_seq, np.float64)
+    P, n, H, D = q.shape
+    G = k.shape[2]
+    scale = 1.0 / math.sqrt(D) if scale is None else scale
+    m = np.full((P, H, n), -np.inf)
+    l = np.zeros((P, H, n))
+    acc = np.zeros((P, H, n, D))
+    held_k, held_v = [k[r] for r in range(P)], [v[r] for r in range(P)]
+    held_id = list(range(P))
+    sent = 0
+    for t in range(P):
+        for r in range(P):
+            j = held_id[r]
+            rows = r * n + np.arange(n)
+            keys = j * n + np.arange(n)
+            visible = keys[None, :] <= rows[:, None]            # [row][key]
+            if not visible.any():
+                continue
+            for h in range(H):
+                g = _kv_head(h, H, G)
+                s = scale * (q[r, :, h, :] @ held_k[r][:, g, :].T)
+                s = np.where(visible, s, -np.inf)
+                m_step = s.max(axis=1)
+                m_new = np.maximum(m[r, h], m_step)
+                keep = np.where(np.isfinite(m_new), np.exp(m[r, h] - m_new), 0.0)
+                p = np.where(visible, np.exp(s - m_new[:, None]), 0.0)
+                acc[r, h] = acc[r, h] * keep[:, None] + p @ held_v[r][:, g, :]
+                l[r, h] = l[r, h] * keep + p.sum(axis=1)
+                m[r, h] = m_new
+        if t < P - 1:   # every rank passes the shard it holds to the next rank
+            held_k = [held_k[(r - 1) % P] for r in range(P)]
+            held_v = [held_v[(r - 1) % P] for r in range(P)]
+            held_id = [held_id[(r - 1) % P] for r in range(P)]
+            sent += n * 2 * G * D * 2
+    o = (acc / l[..., None]).transpose(0, 2, 1, 3)             # [P][n][H][D]
+    lse = m + np.log(l)
+    return o, lse, sent
+
+
+def ring_volume_bytes(S: int, P: int, G: int, D: int, elem_bytes: int = 2):
+    """Bytes one rank sends in ring attention's forward: its K/V shard, forwarded P - 1
+    times, (P - 1) * (S/P) * 2G * D elements."""
+    return (P - 1) * (S // P) * 2 * G * D * elem_bytes

@@ -474,3 +474,30 @@ def test_layer_backward_matches_torch_autograd():
     assert np.allclose(dw, tw.grad.numpy(), rtol=0, atol=1e-10)
     assert np.allclose(dwo, two.grad.numpy(), rtol=0, atol=1e-10)
     assert np.allclose(do_seq, o.grad.numpy().reshape(S, H, D), rtol=0, atol=1e-10)
+
+
+@pytest.mark.parametrize("S,P,H,G,D", [(16, 4, 2, 2, 4), (24, 3, 4, 2, 8), (8, 1, 2, 1, 4),
+                                       (32, 8, 8, 8, 4)])
+def test_ring_attention_equals_unsharded_causal_attention(S, P, H, G, D):
+    """The ring's online merge over shards reaches exactly the plain per-row softmax of the
+    whole sequence (up to rounding), and its lse too."""
+    r = _rng(41)
+    q, k, v = (r.standard_normal((S, n, D)) for n in (H, G, G))
+    o, lse, sent = O.ring_attention(q.reshape(P, S // P, H, D), k.reshape(P, S // P, G, D),
+                                    v.reshape(P, S // P, G, D))
+    ro, rl = O.causal_attention(q, k, v)
+    assert np.allclose(o.reshape(S, H, D), ro, rtol=0, atol=1e-12)
+    assert np.allclose(lse.transpose(1, 0, 2).reshape(H, S), rl, rtol=0, atol=1e-12)
+    assert sent == O.ring_volume_bytes(S, P, G, D)
+
+
+def test_ring_versus_ulysses_volume():
+    """Per-rank bytes: ring (P-1)(S/P)2G D against Ulysses' two all-to-alls
+    (S/P)(2H+2G)D (P-1)/P, so ring / Ulysses = P G / (H + G): P/2 for multi-head attention
+    (G = H), P/5 under 4:1 GQA (1.6 at P = 8 for the 8B head shape)."""
+    S, P, D = 131072, 8, 128
+    for H, G, ratio in ((32, 32, P / 2), (32, 8, P / 5)):
+        ring = O.ring_volume_bytes(S, P, G, D)
+        uly = sum(O.a2a_volume_bytes(S, P, H, G, D))
+        assert ring == (P - 1) * (S // P) * 2 * G * D * 2
+        assert abs(ring / uly - ratio) < 1e-12
