@@ -216,6 +216,29 @@ uint64_t ulysses_bytes_moved(uly_plan plan);
 uly_status ulysses_a2a_volume(const uly_config *cfg, uint64_t *seq_to_head_bytes,
                               uint64_t *head_to_seq_bytes);
 
+/* Ring attention, the comparator the Ulysses-trick page sets against (para 3: its per-GPU
+ * volume is O(hidden * S), against Ulysses' O(hidden * S / P)), run on the same virtual
+ * ranks so that its exchange and its time can be measured beside the all-to-alls.
+ *
+ * The sequence stays sharded: q_seq [P][S/P][H][D], k_seq, v_seq [P][S/P][G][D] (bf16; rank
+ * r holds tokens [r*S/P, (r+1)*S/P), RoPE already applied by the caller).  In step
+ * t = 0 .. P-1 every rank r attends its queries to the K/V shard it holds, (r - t) mod P,
+ * with the causal mask on global positions, and merges the result into its running softmax
+ * state; then every rank passes the shard it holds to rank r + 1 (a device copy: the
+ * ring's communication).  Output o_seq [P][S/P][H][D] (bf16) and lse [P][H][S/P] (fp32,
+ * natural log) equal causal attention of the whole sequence.
+ * workspace: ulysses_ring_workspace_bytes(plan) bytes of device memory (two K/V ring
+ * buffers and the fp32 running state); contents on entry do not matter.
+ * Every launch adds the exchange's read + write bytes to ulysses_bytes_moved. */
+size_t ulysses_ring_workspace_bytes(uly_plan plan);
+uly_status ulysses_ring_attn_fwd(uly_plan plan, const void *q_seq, const void *k_seq,
+                                 const void *v_seq, void *o_seq, float *lse, void *workspace,
+                                 void *stream);
+
+/* Per-rank volume of ring attention's forward: the bytes one rank sends, its K/V shard
+ * forwarded P - 1 times: (P-1) * (S/P) * 2G * D * 2. */
+uly_status ulysses_ring_volume(const uly_config *cfg, uint64_t *bytes);
+
 /* Description of the last error on this thread ("" if none). */
 const char *ulysses_last_error(void);
 

@@ -23,7 +23,8 @@ EXPORTED = ("ulysses_plan", "ulysses_plan_destroy", "ulysses_workspace_bytes",
             "ulysses_qkv_proj", "ulysses_seq_to_head", "ulysses_seq_to_head_heads",
             "ulysses_attn_fwd", "ulysses_attn_bwd", "ulysses_attn_bwd_noalloc",
             "ulysses_head_to_seq", "ulysses_head_to_seq_qkv", "ulysses_qkv_proj_bwd",
-            "ulysses_o_proj", "ulysses_o_proj_bwd",
+            "ulysses_o_proj", "ulysses_o_proj_bwd", "ulysses_ring_workspace_bytes",
+            "ulysses_ring_attn_fwd", "ulysses_ring_volume",
             "ulysses_sync_status", "ulysses_bytes_moved", "ulysses_a2a_volume",
             "ulysses_last_error")
 
@@ -80,6 +81,9 @@ def load_library(path: str = LIB_PATH):
         "ulysses_qkv_proj_bwd": ([vp] * 7, i32),
         "ulysses_o_proj": ([vp] * 5, i32),
         "ulysses_o_proj_bwd": ([vp] * 7, i32),
+        "ulysses_ring_workspace_bytes": ([vp], ctypes.c_size_t),
+        "ulysses_ring_attn_fwd": ([vp] * 8, i32),
+        "ulysses_ring_volume": ([ctypes.POINTER(UlyConfig), ctypes.POINTER(u64)], i32),
         "ulysses_sync_status": ([vp, vp], i32),
         "ulysses_bytes_moved": ([vp], u64),
         "ulysses_a2a_volume": ([ctypes.POINTER(UlyConfig), ctypes.POINTER(u64),
@@ -241,6 +245,22 @@ def ulysses_a2a_volume(cfg: UlyConfig):
     a, b = ctypes.c_uint64(), ctypes.c_uint64()
     _check(load_library().ulysses_a2a_volume(ctypes.byref(cfg), ctypes.byref(a), ctypes.byref(b)))
     return int(a.value), int(b.value)
+
+
+def ulysses_ring_workspace_bytes(plan) -> int:
+    return int(load_library().ulysses_ring_workspace_bytes(plan.handle))
+
+
+def ulysses_ring_attn_fwd(plan, q_seq, k_seq, v_seq, o_seq, lse, workspace, stream=None):
+    _check(load_library().ulysses_ring_attn_fwd(plan.handle, _ptr(q_seq), _ptr(k_seq),
+                                                _ptr(v_seq), _ptr(o_seq), _ptr(lse),
+                                                _ptr(workspace), _stream(stream)))
+
+
+def ulysses_ring_volume(cfg: UlyConfig) -> int:
+    a = ctypes.c_uint64()
+    _check(load_library().ulysses_ring_volume(ctypes.byref(cfg), ctypes.byref(a)))
+    return int(a.value)
 
 
 def ulysses_last_error() -> str:

@@ -462,6 +462,38 @@ uly_status ulysses_a2a_volume(const uly_config* cfg, uint64_t* s2h, uint64_t* h2
   return ULY_OK;
 }
 
+size_t ulysses_ring_workspace_bytes(uly_plan plan) {
+  if (!plan) return 0;
+  return uly::ring_workspace_layout(plan->p).total;
+}
+
+uly_status ulysses_ring_attn_fwd(uly_plan plan, const void* q_seq, const void* k_seq,
+                                 const void* v_seq, void* o_seq, float* lse, void* workspace,
+                                 void* stream) {
+  if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  Plan& p = plan->p;
+  if (p.S == 0) return ULY_OK;
+  if (!q_seq || !k_seq || !v_seq || !o_seq || !lse || !workspace)
+    return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(q_seq) || !aligned16(k_seq) || !aligned16(v_seq) || !aligned16(o_seq) ||
+      !aligned16(lse) || !aligned16(workspace))
+    return fail(ULY_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const uint64_t shard = (uint64_t)(p.S / p.P) * p.G * p.D * 2;
+  p.bytes_moved += (uint64_t)(p.P - 1) * p.P * shard * 2 * 2;   // K and V, read + write
+  return launched(uly::launch_ring_attn(p, q_seq, k_seq, v_seq, o_seq, lse, workspace,
+                                        as_stream(stream)),
+                  "ring attention launch");
+}
+
+uly_status ulysses_ring_volume(const uly_config* cfg, uint64_t* bytes) {
+  uly_status s = validate(cfg);
+  if (s != ULY_OK) return s;
+  if (!bytes) return fail(ULY_ERR_INVALID_ARG, "NULL output pointer");
+  const uint64_t n = (uint64_t)(cfg->seq_len / cfg->P);
+  *bytes = (uint64_t)(cfg->P - 1) * n * 2 * (uint64_t)cfg->n_kv_heads * (uint64_t)cfg->head_dim * 2;
+  return ULY_OK;
+}
+
 const char* ulysses_last_error(void) { return uly::g_err; }
 
 }  // extern "C"

@@ -18,6 +18,14 @@
 //     (so a backward pass can form dO.O to ~16 bits), and lse at the end;
 //   * causal tile skipping: Q0 sees KV tiles 0..m0/128, Q1 one more.
 // TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D) of 512 columns.
+//
+// The same kernel, instantiated with kRing, runs one step of ring attention (the pages'
+// comparator, "Snowflake's Ulysses trick ..." para 3) on the virtual ranks: the sequence
+// stays sharded, rank r holds its queries [S/P][H][D] and, in step t, the K/V shard
+// r - t (ranks r < t hold shards after theirs, which the causal mask hides entirely, and
+// do not run).  Step 0 is the causal diagonal block; later steps are full blocks.  The
+// running (max, sum, fp32 accumulator) state of every row is kept in HBM between steps and
+// loaded into TMEM before the first P V; rank r writes its normalised output at step r.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -51,6 +59,11 @@ struct FwdArgs {
   int* status;
   uint64_t limit_ns;
   uint32_t flags;
+  // ring steps only: S is the shard length S/P, hl = H, gl = G
+  int ring_t;
+  float* acc;      // [P][S/P][H][D] fp32, unnormalised output
+  float* mstate;   // [P][H][S/P] running max (log2 domain, scale applied)
+  float* lstate;   // [P][H][S/P] running sum
 };
 
 __device__ __forceinline__ float lg2_approx(float x) {
@@ -59,7 +72,7 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
-template <int D>
+template <int D, bool kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdArgs a) {
@@ -84,15 +97,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Block -> (rank, local query head, 256-row block), heaviest blocks first.
   const int per_rank = a.hl * a.n_mb;
-  const int r = blockIdx.x / per_rank;
-  const int rem = blockIdx.x - r * per_rank;
+  const int rb = (int)blockIdx.x / per_rank;                // rank within the launch
+  const int r = (kRing ? a.ring_t : 0) + rb;
+  const bool full_blk = kRing && a.ring_t > 0;   // a shard before this rank's own: no mask
+  const int rem = (int)blockIdx.x - rb * per_rank;
   const int mb = a.n_mb - 1 - rem / a.hl;
   const int hh = rem % a.hl;
   const int gg = hh / a.group;
   const int m0 = mb * 2 * BM;
   const int n_kv = (a.S + BN - 1) / BN;
-  const int n0 = min(m0 / BN + 1, n_kv);
-  const int n1 = min(m0 / BN + 2, n_kv);
+  const int n0 = full_blk ? n_kv : min(m0 / BN + 1, n_kv);
+  const int n1 = full_blk ? n_kv : min(m0 / BN + 2, n_kv);
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -180,7 +195,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tbase + 2 * BN + t * D, tbase + t * BN + kk * 8, vb + ((kk * 16 * 128) >> 4),
-                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                 idesc_pv, (j > 0 || kk > 0 || full_blk) ? 1u : 0u);
         return true;
       };
       for (int j = 0; alive && j < n1; ++j) {
@@ -223,6 +238,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t to = tbase + ((uint32_t)lane_base << 16) + 2 * BN + t * D;
     const float sl2 = a.scale_log2;
     float m_used = -INFINITY, l = 0.f;
+    // row offsets: output / accumulator [P][S][H][D], lse / state [P][H][S]
+    auto srow = [&]() { return ((size_t)r * a.hl + hh) * a.S + row_g; };
+    auto orow_off = [&]() { return (((size_t)r * a.S + row_g) * a.hl + hh) * D; };
+    if (full_blk) {
+      const bool live = row_g < a.S;
+      // the state the rank's earlier steps left: O into TMEM before the first P V
+      if (live) {
+        m_used = a.mstate[srow()];
+        l = a.lstate[srow()];
+      }
+      const float4* arow = reinterpret_cast<const float4*>(a.acc + orow_off());
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float4 x = live ? arow[8 * c + e] : make_float4(0.f, 0.f, 0.f, 0.f);
+          o[4 * e] = __float_as_uint(x.x);
+          o[4 * e + 1] = __float_as_uint(x.y);
+          o[4 * e + 2] = __float_as_uint(x.z);
+          o[4 * e + 3] = __float_as_uint(x.w);
+        }
+        tmem_st32(to + 32 * c, o);
+      }
+    }
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[t], j & 1, wc));
@@ -232,13 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(ts + 32 * c, s[c]);
       const int kbase = j * BN;
-      if (kbase + BN - 1 > m0 + t * BM || kbase + BN > a.S) {
+      if ((!full_blk && kbase + BN - 1 > m0 + t * BM) || kbase + BN > a.S) {
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const int kp = kbase + 32 * c + i;
-            if (kp > row_g || kp >= a.S) s[c][i] = __float_as_uint(-INFINITY);
+            if ((!full_blk && kp > row_g) || kp >= a.S) s[c][i] = __float_as_uint(-INFINITY);
           }
       }
       // row max: four independent chains of 3-input max
@@ -252,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_new = fmaxf(m_used, mx * sl2);
       float alpha = 1.f;
       bool rescale = false;
-      if (j == 0) {
+      if (j == 0 && !full_blk) {
         m_used = m_new;
       } else if (m_new > m_used + 8.f) {
         alpha = ex2_approx(m_used - m_new);
@@ -298,11 +338,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&p_full[t]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0, wc));
-    if (ok) {
+    if (ok && kRing && a.ring_t != r) {
+      // not this rank's last step: keep the state for the next one
+      tc_fence_after();
+      const bool live = row_g < a.S;
+      float4* arow = reinterpret_cast<float4*>(a.acc + orow_off());
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(to + 32 * c, o);
+        if (live) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            arow[8 * c + e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                          __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+        }
+      }
+      if (live) {
+        a.mstate[srow()] = m_used;
+        a.lstate[srow()] = l;
+      }
+    } else if (ok) {
       tc_fence_after();
       const float inv_l = 1.f / l;
-      const size_t orow_off = (((size_t)r * a.S + row_g) * a.hl + hh) * D;
-      __nv_bfloat16* orow = a.o + orow_off;
+      __nv_bfloat16* orow = a.o + orow_off();
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -326,14 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lw[e] = pack_bf16x2(__uint_as_float(o[8 * j + 2 * e]) * inv_l - h.x,
                                     __uint_as_float(o[8 * j + 2 * e + 1]) * inv_l - h.y);
               }
-              *reinterpret_cast<uint4*>(a.o_lo + orow_off + 32 * c + 8 * j) =
+              *reinterpret_cast<uint4*>(a.o_lo + orow_off() + 32 * c + 8 * j) =
                   make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
           }
         }
       }
-      if (row_g < a.S)
-        a.lse[((size_t)r * a.hl + hh) * a.S + row_g] = (m_used + lg2_approx(l)) * 0.6931471805599453f;
+      if (row_g < a.S) a.lse[srow()] = (m_used + lg2_approx(l)) * 0.6931471805599453f;
     }
   }
 
@@ -373,12 +431,93 @@ cudaError_t launch_fwd_d(const Plan& p, const void* q, const void* k, const void
   a.status = p.status;
   a.limit_ns = p.limit_ns;
   a.flags = p.cfg.flags;
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Layout<D>::kBytes);
+  a.ring_t = 0;
+  a.acc = a.mstate = a.lstate = nullptr;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kBytes);
   if (e != cudaSuccess) return e;
   const int64_t blocks = (int64_t)p.P * hl * a.n_mb;
-  attn_fwd_kernel<D><<<(unsigned)blocks, kThreads, Layout<D>::kBytes, st>>>(tq, tk, tv, a);
+  attn_fwd_kernel<D, false><<<(unsigned)blocks, kThreads, Layout<D>::kBytes, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
+}
+
+// Ring exchange: every rank passes the K and V shard it holds to rank r + 1:
+// dst[(r + 1) mod P] = src[r], 16-byte vectors.
+__global__ void __launch_bounds__(256) ring_pass_kernel(const uint4* __restrict__ k_src,
+                                                        const uint4* __restrict__ v_src,
+                                                        uint4* __restrict__ k_dst,
+                                                        uint4* __restrict__ v_dst, int P,
+                                                        int64_t shard8) {
+  const int64_t total = (int64_t)P * shard8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / shard8;
+    const int64_t e = i - r * shard8;
+    const int64_t d = (r + 1 == P ? 0 : r + 1) * shard8 + e;
+    k_dst[d] = __ldcs(k_src + i);
+    v_dst[d] = __ldcs(v_src + i);
+  }
+}
+
+template <int D>
+cudaError_t launch_ring_d(const Plan& p, const void* q_seq, const void* k_seq, const void* v_seq,
+                          void* o_seq, float* lse, void* workspace, cudaStream_t st) {
+  const int n = (int)(p.S / p.P);
+  const RingWorkspace ws = ring_workspace_layout(p);
+  char* wsb = static_cast<char*>(workspace);
+  void* kbuf[2] = {wsb + ws.k[0], wsb + ws.k[1]};
+  void* vbuf[2] = {wsb + ws.v[0], wsb + ws.v[1]};
+  const char* err = nullptr;
+  CUtensorMap tq;
+  const uint64_t dq[4] = {(uint64_t)D, (uint64_t)p.H, (uint64_t)n, (uint64_t)p.P};
+  const uint64_t sq[3] = {(uint64_t)D * 2, (uint64_t)p.H * D * 2, (uint64_t)n * p.H * D * 2};
+  const uint64_t dk[4] = {(uint64_t)D, (uint64_t)p.G, (uint64_t)n, (uint64_t)p.P};
+  const uint64_t sk[3] = {(uint64_t)D * 2, (uint64_t)p.G * D * 2, (uint64_t)n * p.G * D * 2};
+  if (!make_tmap_4d_bf16(&tq, q_seq, dq, sq, 64, BM, &err)) return cudaErrorInvalidValue;
+  FwdArgs a;
+  a.o = static_cast<__nv_bfloat16*>(o_seq);
+  a.o_lo = nullptr;
+  a.lse = lse;
+  a.S = n;
+  a.hl = p.H;
+  a.gl = p.G;
+  a.group = p.H / p.G;
+  a.n_mb = (n + 2 * BM - 1) / (2 * BM);
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.status = p.status;
+  a.limit_ns = p.limit_ns;
+  a.flags = 0;
+  a.acc = reinterpret_cast<float*>(wsb + ws.acc);
+  a.mstate = reinterpret_cast<float*>(wsb + ws.m);
+  a.lstate = reinterpret_cast<float*>(wsb + ws.l);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<D>::kBytes);
+  if (e != cudaSuccess) return e;
+  const int64_t shard8 = (int64_t)n * p.G * D / 8;
+  const int64_t cap = (int64_t)num_sms(p.device) * 8;
+  const unsigned pass_blocks = (unsigned)std::min<int64_t>((p.P * shard8 + 255) / 256, cap);
+  for (int t = 0; t < p.P; ++t) {
+    const void* kc = t == 0 ? k_seq : kbuf[t % 2];
+    const void* vc = t == 0 ? v_seq : vbuf[t % 2];
+    CUtensorMap tk, tv;
+    if (!make_tmap_4d_bf16(&tk, kc, dk, sk, 64, BN, &err) ||
+        !make_tmap_4d_bf16(&tv, vc, dk, sk, 64, BN, &err))
+      return cudaErrorInvalidValue;
+    a.ring_t = t;
+    const int64_t blocks = (int64_t)(p.P - t) * p.H * a.n_mb;
+    attn_fwd_kernel<D, true><<<(unsigned)blocks, kThreads, Layout<D>::kBytes, st>>>(tq, tk, tv, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (t + 1 < p.P) {
+      ring_pass_kernel<<<pass_blocks, 256, 0, st>>>(
+          static_cast<const uint4*>(kc), static_cast<const uint4*>(vc),
+          static_cast<uint4*>(kbuf[(t + 1) % 2]), static_cast<uint4*>(vbuf[(t + 1) % 2]), p.P,
+          shard8);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -387,6 +526,29 @@ cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const v
                             void* o_lo, float* lse, cudaStream_t st) {
   if (p.D == 64) return launch_fwd_d<64>(p, q, k, v, o, o_lo, lse, st);
   return launch_fwd_d<128>(p, q, k, v, o, o_lo, lse, st);
+}
+
+RingWorkspace ring_workspace_layout(const Plan& p) {
+  const size_t S = (size_t)p.S, H = p.H, G = p.G, D = p.D;
+  auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
+  RingWorkspace w;
+  size_t off = 0;
+  for (int i = 0; i < 2; ++i) {
+    w.k[i] = off; off += al(S * G * D * 2);
+    w.v[i] = off; off += al(S * G * D * 2);
+  }
+  w.acc = off; off += al(S * H * D * 4);
+  w.m = off;   off += al(S * H * 4);
+  w.l = off;   off += al(S * H * 4);
+  w.total = off;
+  return w;
+}
+
+cudaError_t launch_ring_attn(const Plan& p, const void* q_seq, const void* k_seq,
+                             const void* v_seq, void* o_seq, float* lse, void* workspace,
+                             cudaStream_t st) {
+  if (p.D == 64) return launch_ring_d<64>(p, q_seq, k_seq, v_seq, o_seq, lse, workspace, st);
+  return launch_ring_d<128>(p, q_seq, k_seq, v_seq, o_seq, lse, workspace, st);
 }
 
 }  // namespace uly

@@ -57,6 +57,16 @@ cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const v
 
 // Workspace layout of the backward pass (byte offsets, each 256-aligned): fp32 dQ
 // accumulator, fp32 row terms, fp16 copies of q, dO, k, v.
+// Ring attention: K/V ring buffers (two sets, the steps alternate), the fp32 output
+// accumulator and the running max / sum of every row.
+struct RingWorkspace {
+  size_t k[2], v[2], acc, m, l, total;
+};
+RingWorkspace ring_workspace_layout(const Plan& p);
+cudaError_t launch_ring_attn(const Plan& p, const void* q_seq, const void* k_seq,
+                             const void* v_seq, void* o_seq, float* lse, void* workspace,
+                             cudaStream_t st);
+
 struct BwdWorkspace {
   size_t dq_acc, delta, q16, do16, k16, v16, total;
 };

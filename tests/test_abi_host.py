@@ -77,3 +77,9 @@ def test_null_plan_is_rejected(lib):
         U.ulysses_attn_fwd(Fake(), 0, 0, 0, 0, 0, stream=0)
     assert ei.value.status == U.ULY_ERR_INVALID_ARG
     assert "plan" in U.ulysses_last_error()
+
+
+@pytest.mark.parametrize("S,P,H,G,D", [(131072, 8, 32, 8, 128), (1024, 4, 8, 8, 64), (8, 1, 2, 1, 64)])
+def test_ring_volume_matches_oracle_closed_form(lib, S, P, H, G, D):
+    assert U.ulysses_ring_volume(U.make_config(S, P, 4096, H, G, D)) == \
+        O.ring_volume_bytes(S, P, G, D)
