@@ -445,6 +445,42 @@ def run_ours(args):
                  "qkv_proj_bwd_tflops": 2 * proj_f / (lper["qkv_proj_bwd"] * 1e-3) / 1e12,
                  "launches_per_step": 1 + 1 + 1 + 1 + 2 + 3 + 1 + 2}
 
+    # Ring attention (the pages' comparator) on the same virtual ranks and tokens: its
+    # forward with the K/V exchange, beside the Ulysses forward path (seq->head, attention,
+    # head->seq of O), and the per-rank volumes of the two exchanges.
+    ring = None
+    if not args.no_ring:
+        n = S // P
+        q_s = torch.randn((P, n, H, D), generator=gen, device=dev).mul_(1.28).to(bf)
+        k_s = torch.randn((P, n, G, D), generator=gen, device=dev).mul_(1.28).to(bf)
+        v_s = torch.randn((P, n, G, D), generator=gen, device=dev).mul_(1.28).to(bf)
+        o_s = torch.empty((P, n, H, D), dtype=bf, device=dev)
+        lse_s = torch.empty((P, H, n), dtype=torch.float32, device=dev)
+        rws = torch.empty(U.ulysses_ring_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+        for _ in range(args.warmup):
+            U.ulysses_ring_attn_fwd(plan, q_s, k_s, v_s, o_s, lse_s, rws, sid)
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        b0 = U.ulysses_bytes_moved(plan)
+        r0.record(stream)
+        for _ in range(args.steps):
+            U.ulysses_ring_attn_fwd(plan, q_s, k_s, v_s, o_s, lse_s, rws, sid)
+        r1.record(stream)
+        torch.cuda.synchronize()
+        st = U.ulysses_sync_status(plan, sid)
+        if st != U.ULY_OK:
+            raise RuntimeError("device status %d: %s" % (st, U.ulysses_last_error()))
+        rms = r0.elapsed_time(r1) / args.steps
+        cfg = U.make_config(S, P, hidden, H, G, D, rope_theta=theta)
+        rv = U.ulysses_ring_volume(cfg)
+        uv = sum(U.ulysses_a2a_volume(cfg))
+        uly_fwd_ms = avg["seq_to_head"] + avg["attn_fwd"] + avg["head_to_seq_o"]
+        ring = {"ms": rms, "tflops": fwd_f / (rms * 1e-3) / 1e12,
+                "exchange_bytes_moved_per_call": (U.ulysses_bytes_moved(plan) - b0) // args.steps,
+                "volume_per_rank_bytes": rv, "ulysses_volume_per_rank_bytes": uv,
+                "volume_ratio_ring_over_ulysses": rv / uv,
+                "ulysses_fwd_path_ms": uly_fwd_ms, "launches_per_call": 2 * P - 1}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         f, s, desc = oracle_sample(S, H, D, 6144)
@@ -473,7 +509,7 @@ def run_ours(args):
             "seq_to_head_gbs": s2h_gbs, "peaks": peaks, "peaks_source": peak_kind,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
-            "layer_train_step": layer,
+            "layer_train_step": layer, "ring_attention": ring,
         }
         print(json.dumps(line))
     plan.close()
@@ -490,6 +526,7 @@ def main():
     ap.add_argument("--seq", type=int, default=0, help="override S (quick checks only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-layer", action="store_true")
+    ap.add_argument("--no-ring", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.seq:
