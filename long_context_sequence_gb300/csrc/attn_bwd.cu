@@ -14,7 +14,10 @@
 //   bwd_main  one CTA per (rank, KV head, 128-key block).  Work items are (64-row query
 //             tile, query head of the group) pairs from the diagonal on.  Items alternate
 //             between two TMEM regions so that one item's tensor work overlaps the other's
-//             element-wise work; the MMA warp issues MMA2(it) then MMA1(it+2):
+//             element-wise work.  Two threads issue the MMAs (one thread issues a
+//             tcgen05.mma about every 58 cycles whatever its size, and these are small):
+//             issuer A the MMA1s and dQ^T of both regions, issuer B every dV and dK (the
+//             accumulators both regions share, so one thread orders them):
 //               MMA1   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 64 rows)
 //               8 warps per region, thread = key row, warpgroup = 32 query columns:
 //                      P^T = scale*exp(S^T scale - lse) -> TMEM (fp16, over dP^T),
@@ -42,8 +45,8 @@ constexpr int BN = 128;   // keys per CTA
 constexpr int BMI = 64;   // query rows per item
 constexpr int NST = 4;    // Q/dO stages
 constexpr int kRegionThreads = 256;          // 8 warps per TMEM region
-constexpr int kTmaWarp = 16, kMmaWarp = 17;
-constexpr int kThreads = 576;
+constexpr int kTmaWarp = 16, kMmaWarp = 17, kAccWarp = 18;
+constexpr int kThreads = 608;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 128 * 128;   // [128 rows][128 bytes]
 constexpr int kBox64 = 64 * 128;  // [64 rows][128 bytes]
@@ -129,7 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_free = s_full + 6;            // [2]
   uint64_t* acc_done = s_full + 8;
   uint64_t* drain = s_full + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 10);
+  uint64_t* pv_done = s_full + 10;           // [2] dV, dK of a region's item done
+  uint64_t* drain_acc = s_full + 12;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 13);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
 
@@ -156,6 +161,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
+    mbar_init(&pv_done[0], 1);
+    mbar_init(&pv_done[1], 1);
+    mbar_init(drain_acc, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -219,19 +227,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(&qd_full[it % NST], (it / NST) & 1, a.limit_ns);
     }
   } else if (warp == kMmaWarp) {
+    // Issuer A: MMA1 and dQ^T, which write only their own region's columns.
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_f16(BN, BMI, false, false);  // S^T, dP^T (N = 64)
       constexpr uint32_t id_q = idesc_f16(128, BMI, true, true);   // dQ^T (M = d, N = 64)
-      constexpr uint32_t id_kv = idesc_f16(BN, D, false, true);    // dV, dK (K = 64 rows)
       // Descriptors are built once; a K-step adds its byte offset / 16 to the address
       // field (no carry: every smem address here is below 2^18).
       const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
       const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
       const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), kBox, 1024);
+      // MMA1 of item it over region X.  Its S^T columns held dQ^T(it-2) (read out by the
+      // element-wise warps: dq_free) and its dP^T columns held P^T(it-2), which issuer B's
+      // dV(it-2) read (pv_done).
       auto mma1 = [&](int it) -> bool {
         const int X = it & 1, st = it % NST;
         if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) return false;
         if (it >= 2 && !mbar_wait(&dq_free[X], ((it - 2) >> 1) & 1, wc)) return false;
+        if (it >= 2 && !mbar_wait(&pv_done[X], ((it - 2) >> 1) & 1, wc)) return false;
         tc_fence_after();
         const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + L::kQ + st * L::kItem), 16, 1024);
         const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO + st * L::kItem), 16, 1024);
@@ -250,46 +262,62 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&s_full[X]);
         return true;
       };
-      auto mma2 = [&](int it) -> bool {
-        const int X = it & 1, st = it % NST;
+      // dQ^T of item it over region X's S^T columns
+      auto mma_dq = [&](int it) -> bool {
+        const int X = it & 1;
         if (!mbar_wait(&p_full[X], (it >> 1) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t sQ = smem_u32(smem + L::kQ + st * L::kItem);
-        const uint32_t sDO = smem_u32(smem + L::kDO + st * L::kItem);
-        const uint32_t sDS = smem_u32(smem + L::kDS + X * kBox);
-        const uint64_t dQ_mn = sdesc_sw128(sQ, kBox64, 1024), dDO_mn = sdesc_sw128(sDO, kBox64, 1024);
-        const uint64_t dDS_mn = sdesc_sw128(sDS, kBox, 1024), dDS_k = sdesc_sw128(sDS, 16, 1024);
-        // dQ^T (over this region's S^T columns) first: its read-out overlaps dV and dK.
+        const uint64_t dDS_mn = sdesc_sw128(smem_u32(smem + L::kDS + X * kBox), kBox, 1024);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ss(tbase + 128 * X, dK_mn + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), id_q,
                  kk > 0 ? 1u : 0u);
         mma_commit(&dq_full[X]);
+        return true;
+      };
+      // Pairs, one item per region: dQ^T of both, then MMA1 of the next two.  (Serving
+      // the regions in whatever order their barriers complete, by polling both, was
+      // slower: the spinning issuer costs more than the order it saves.)
+      bool alive = mbar_wait(kv_full, 0, wc);
+      for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma1(it);
+      for (int it = 0; alive && it < n_items; it += 2) {
+        alive = mma_dq(it);
+        if (alive && it + 1 < n_items) alive = mma_dq(it + 1);
+        if (alive && it + 2 < n_items) alive = mma1(it + 2);
+        if (alive && it + 3 < n_items) alive = mma1(it + 3);
+      }
+      mma_commit(drain);
+      mbar_drain(drain, 0, a.limit_ns);
+    }
+  } else if (warp == kAccWarp) {
+    // Issuer B: every dV and dK MMA, in item order (the two accumulators are shared by both
+    // regions, so one thread issues all MMAs into them).
+    if (lane == 0) {
+      constexpr uint32_t id_kv = idesc_f16(BN, D, false, true);    // dV, dK (K = 64 rows)
+      bool alive = true;
+      for (int it = 0; alive && it < n_items; ++it) {
+        const int X = it & 1, st = it % NST;
+        if (!mbar_wait(&p_full[X], (it >> 1) & 1, wc)) { alive = false; break; }
+        tc_fence_after();
+        const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + L::kQ + st * L::kItem), kBox64, 1024);
+        const uint64_t dDO_mn = sdesc_sw128(smem_u32(smem + L::kDO + st * L::kItem), kBox64, 1024);
+        const uint64_t dDS_k = sdesc_sw128(smem_u32(smem + L::kDS + X * kBox), 16, 1024);
+        // dV += P^T dO (A = P^T from TMEM: rows 16kk.. of warpgroup kk/2, packed fp16)
 #pragma unroll
         for (int kk = 0; kk < BMI / 16; ++kk)
           mma_ts(tbase + 256, tbase + 128 * X + 64 + 32 * (kk / 2) + 8 * (kk % 2),
                  dDO_mn + ((kk * 2048) >> 4), id_kv, (it > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q (A = dS [keys][rows], K-major)
 #pragma unroll
         for (int kk = 0; kk < BMI / 16; ++kk)
           mma_ss(tbase + 256 + D, dDS_k + ((kk * 32) >> 4), dQ_mn + ((kk * 2048) >> 4), id_kv,
                  (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&pv_done[X]);
         mma_commit(&qd_empty[st]);
-        return true;
-      };
-      // Items are issued in pairs, one per region: MMA2 of both, then MMA1 of the next
-      // two.  MMA1(it+2) waits for region X's dQ^T read-out; by then the other region's
-      // MMA2 already sits in the tensor pipe, so that latency is hidden behind it.
-      bool alive = mbar_wait(kv_full, 0, wc);
-      for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma1(it);
-      for (int it = 0; alive && it < n_items; it += 2) {
-        alive = mma2(it);
-        if (alive && it + 1 < n_items) alive = mma2(it + 1);
-        if (alive && it + 2 < n_items) alive = mma1(it + 2);
-        if (alive && it + 3 < n_items) alive = mma1(it + 3);
       }
       if (alive) mma_commit(acc_done);
-      mma_commit(drain);
-      mbar_drain(drain, 0, a.limit_ns);
+      mma_commit(drain_acc);
+      mbar_drain(drain_acc, 0, a.limit_ns);
     }
   } else {
     // 16 element-wise warps: warps [8X, 8X+8) serve TMEM region X (items X, X+2, ...);
