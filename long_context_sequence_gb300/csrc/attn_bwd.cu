@@ -16,8 +16,8 @@
 //             between two TMEM regions so that one item's tensor work overlaps the other's
 //             element-wise work.  Two threads issue the MMAs (one thread issues a
 //             tcgen05.mma about every 58 cycles whatever its size, and these are small):
-//             issuer A the MMA1s and dQ^T of both regions, issuer B every dV and dK (the
-//             accumulators both regions share, so one thread orders them):
+//             issuer A S^T and dQ^T of both regions, issuer B dP^T and every dV and dK
+//             (the accumulators both regions share, so one thread orders them):
 //               MMA1   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 64 rows)
 //               8 warps per region, thread = key row, warpgroup = 32 query columns:
 //                      P^T = scale*exp(S^T scale - lse) -> TMEM (fp16, over dP^T),
@@ -132,8 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dq_free = s_full + 6;            // [2]
   uint64_t* acc_done = s_full + 8;
   uint64_t* drain = s_full + 9;
-  uint64_t* pv_done = s_full + 10;           // [2] dV, dK of a region's item done
-  uint64_t* drain_acc = s_full + 12;
+  uint64_t* drain_acc = s_full + 10;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 13);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
@@ -154,15 +153,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&qd_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
+      mbar_init(&s_full[i], 2);    // S^T (issuer A) and dP^T (issuer B)
       mbar_init(&p_full[i], 1);
       mbar_init(&dq_full[i], 1);
       mbar_init(&dq_free[i], 1);
     }
     mbar_init(acc_done, 1);
     mbar_init(drain, 1);
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
     mbar_init(drain_acc, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -227,37 +224,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(&qd_full[it % NST], (it / NST) & 1, a.limit_ns);
     }
   } else if (warp == kMmaWarp) {
-    // Issuer A: MMA1 and dQ^T, which write only their own region's columns.
+    // Issuer A: S^T and dQ^T of both regions (both over a region's S^T columns).
     if (lane == 0) {
-      constexpr uint32_t id_s = idesc_f16(BN, BMI, false, false);  // S^T, dP^T (N = 64)
+      constexpr uint32_t id_s = idesc_f16(BN, BMI, false, false);  // S^T (N = 64)
       constexpr uint32_t id_q = idesc_f16(128, BMI, true, true);   // dQ^T (M = d, N = 64)
       // Descriptors are built once; a K-step adds its byte offset / 16 to the address
       // field (no carry: every smem address here is below 2^18).
       const uint64_t dK_k = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
-      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
       const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), kBox, 1024);
-      // MMA1 of item it over region X.  Its S^T columns held dQ^T(it-2) (read out by the
-      // element-wise warps: dq_free) and its dP^T columns held P^T(it-2), which issuer B's
-      // dV(it-2) read (pv_done).
-      auto mma1 = [&](int it) -> bool {
+      // S^T of item it over region X's S^T columns, which held dQ^T(it-2) until the
+      // element-wise warps read it out (dq_free).
+      auto mma_s = [&](int it) -> bool {
         const int X = it & 1, st = it % NST;
         if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) return false;
         if (it >= 2 && !mbar_wait(&dq_free[X], ((it - 2) >> 1) & 1, wc)) return false;
-        if (it >= 2 && !mbar_wait(&pv_done[X], ((it - 2) >> 1) & 1, wc)) return false;
         tc_fence_after();
         const uint64_t dQ_k = sdesc_sw128(smem_u32(smem + L::kQ + st * L::kItem), 16, 1024);
-        const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO + st * L::kItem), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offa = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
           const uint32_t offb = ((kk / 4) * kBox64 + (kk % 4) * 32) >> 4;
           mma_ss(tbase + 128 * X, dK_k + offa, dQ_k + offb, id_s, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t offa = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
-          const uint32_t offb = ((kk / 4) * kBox64 + (kk % 4) * 32) >> 4;
-          mma_ss(tbase + 128 * X + 64, dV_k + offa, dDO_k + offb, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[X]);
         return true;
@@ -275,26 +262,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&dq_full[X]);
         return true;
       };
-      // Pairs, one item per region: dQ^T of both, then MMA1 of the next two.  (Serving
+      // Pairs, one item per region: dQ^T of both, then S^T of the next two.  (Serving
       // the regions in whatever order their barriers complete, by polling both, was
       // slower: the spinning issuer costs more than the order it saves.)
       bool alive = mbar_wait(kv_full, 0, wc);
-      for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma1(it);
+      for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma_s(it);
       for (int it = 0; alive && it < n_items; it += 2) {
         alive = mma_dq(it);
         if (alive && it + 1 < n_items) alive = mma_dq(it + 1);
-        if (alive && it + 2 < n_items) alive = mma1(it + 2);
-        if (alive && it + 3 < n_items) alive = mma1(it + 3);
+        if (alive && it + 2 < n_items) alive = mma_s(it + 2);
+        if (alive && it + 3 < n_items) alive = mma_s(it + 3);
       }
       mma_commit(drain);
       mbar_drain(drain, 0, a.limit_ns);
     }
   } else if (warp == kAccWarp) {
-    // Issuer B: every dV and dK MMA, in item order (the two accumulators are shared by both
-    // regions, so one thread issues all MMAs into them).
+    // Issuer B: dP^T of both regions and every dV and dK, in item order.  dP^T(it+2) goes
+    // over the columns where P^T(it) sat, after dV(it) read it (same thread, in order);
+    // the dV/dK accumulators are shared by both regions, so one thread orders them.
     if (lane == 0) {
+      constexpr uint32_t id_s = idesc_f16(BN, BMI, false, false);  // dP^T (N = 64)
       constexpr uint32_t id_kv = idesc_f16(BN, D, false, true);    // dV, dK (K = 64 rows)
-      bool alive = true;
+      const uint64_t dV_k = sdesc_sw128(smem_u32(smem + L::kV), 16, 1024);
+      auto mma_dp = [&](int it) -> bool {
+        const int X = it & 1, st = it % NST;
+        if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) return false;
+        tc_fence_after();
+        const uint64_t dDO_k = sdesc_sw128(smem_u32(smem + L::kDO + st * L::kItem), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t offa = ((kk / 4) * kBox + (kk % 4) * 32) >> 4;
+          const uint32_t offb = ((kk / 4) * kBox64 + (kk % 4) * 32) >> 4;
+          mma_ss(tbase + 128 * X + 64, dV_k + offa, dDO_k + offb, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&s_full[X]);
+        return true;
+      };
+      bool alive = mbar_wait(kv_full, 0, wc);
+      for (int it = 0; alive && it < 2 && it < n_items; ++it) alive = mma_dp(it);
       for (int it = 0; alive && it < n_items; ++it) {
         const int X = it & 1, st = it % NST;
         if (!mbar_wait(&p_full[X], (it >> 1) & 1, wc)) { alive = false; break; }
@@ -312,8 +317,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BMI / 16; ++kk)
           mma_ss(tbase + 256 + D, dDS_k + ((kk * 32) >> 4), dQ_mn + ((kk * 2048) >> 4), id_kv,
                  (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&pv_done[X]);
         mma_commit(&qd_empty[st]);
+        if (it + 2 < n_items) alive = mma_dp(it + 2);
       }
       if (alive) mma_commit(acc_done);
       mma_commit(drain_acc);
