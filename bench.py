@@ -244,7 +244,9 @@ def run_ours(args):
     sid = stream.cuda_stream
     names = ["qkv_proj", "seq_to_head", "attn_fwd", "head_to_seq_o", "seq_to_head_do",
              "attn_bwd", "head_to_seq_grads"]
-    launches_per_step = 1 + 1 + 1 + 1 + 1 + 3 + 1
+    # qkv_proj, seq_to_head, attn_fwd, head_to_seq (O), seq_to_head (dO), attn_bwd (pre, two
+    # fp16 copies, main, dQ conversion), head_to_seq of the gradients
+    launches_per_step = 1 + 1 + 1 + 1 + 1 + 5 + 1
 
     def step(ev=None, io=None):
         # io: the step's input and output buffers (x, dO_seq, o_seq, dqkv_seq)
@@ -448,7 +450,7 @@ def run_ours(args):
                  "o_proj_tflops": oproj_f / (lper["o_proj"] * 1e-3) / 1e12,
                  "o_proj_bwd_tflops": 2 * oproj_f / (lper["o_proj_bwd"] * 1e-3) / 1e12,
                  "qkv_proj_bwd_tflops": 2 * proj_f / (lper["qkv_proj_bwd"] * 1e-3) / 1e12,
-                 "launches_per_step": 1 + 1 + 1 + 1 + 2 + 3 + 1 + 2}
+                 "launches_per_step": 1 + 1 + 1 + 1 + 2 + 5 + 1 + 2}
 
     # Ring attention (the pages' comparator) on the same virtual ranks and tokens: its
     # forward with the K/V exchange, beside the Ulysses forward path (seq->head, attention,

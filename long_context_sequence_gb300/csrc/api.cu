@@ -65,24 +65,6 @@ int num_sms(int device) {
   return cached[device];
 }
 
-bool make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                       const char** err) {
-  EncodeTiledFn fn = encode_fn(err);
-  if (!fn) return false;
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {row_stride_bytes};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    if (err) *err = "cuTensorMapEncodeTiled (2-D) rejected the layout";
-    return false;
-  }
-  return true;
-}
 
 bool make_tmap_3d_bf16(CUtensorMap* m, const void* base, const uint64_t dims_in[3],
                        const uint64_t strides_bytes[2], uint32_t box0, uint32_t box1,
@@ -130,24 +112,6 @@ uly_status set_error(uly_status s, const char* msg) {
   return fail(s, "%s", msg);
 }
 
-bool make_tmap_4d_f32(CUtensorMap* m, const void* base, const uint64_t dims_in[4],
-                      const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
-                      const char** err) {
-  EncodeTiledFn fn = encode_fn(err);
-  if (!fn) return false;
-  cuuint64_t dims[4] = {dims_in[0], dims_in[1], dims_in[2], dims_in[3]};
-  cuuint64_t strides[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
-  cuuint32_t box[4] = {box0, 1, box2, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) {
-    if (err) *err = "cuTensorMapEncodeTiled (4-D fp32) rejected the layout";
-    return false;
-  }
-  return true;
-}
 
 }  // namespace uly
 

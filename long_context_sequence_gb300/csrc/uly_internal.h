@@ -75,9 +75,6 @@ size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off)
 
 // Tensor maps (TMA descriptors), built on the host through the driver entry point.
 // Returns false and sets *err on failure.
-bool make_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
-                       const char** err);
 // 3-D bf16 map over [parts][rows][x] with byte strides {row, part} and a box of
 // {box0, box1, 1}; 128-byte swizzle, out-of-range elements read as zero.
 bool make_tmap_3d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[3],
@@ -88,11 +85,6 @@ bool make_tmap_3d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[3],
 bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4],
                        const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
                        const char** err);
-
-// 4-D fp32 map without swizzle (box {box0, 1, box2, 1}); used as a TMA reduce target.
-bool make_tmap_4d_f32(CUtensorMap* m, const void* base, const uint64_t dims[4],
-                      const uint64_t strides_bytes[3], uint32_t box0, uint32_t box2,
-                      const char** err);
 
 int num_sms(int device);
 
