@@ -47,7 +47,7 @@ def attn_flops(S, H, D):
 BWD_TRAFFIC = {"bytes": (4.30 + 4.26 + (0.26845 + 0.21484) + (0.26851 + 0.21321) + 17.28 + 8.81
                          + 2.15 + 1.04) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "d2badd2574a9c80a40cc7862094f4cc0eb43e768360923033ccb056959e9c81c"}
+               "source_sha256": "8659c4f2aebc230383f46af7f0fc9951683a97c6552d8b2fcf88ee2fd28e83a4"}
 
 
 def bwd_traffic(seq_len):
