@@ -63,8 +63,10 @@ typedef enum uly_status {
 } uly_status;
 
 /* Plan flags. */
-#define ULY_FLAG_INJECT_STALL 0x1u /* test only: attn_fwd's MMA issuer withholds its first
-                                      score-ready signal, so the bounded waits run out */
+#define ULY_FLAG_INJECT_STALL 0x1u /* test only: in block 0 of ulysses_attn_fwd and
+                                      ulysses_attn_bwd the MMA issuer withholds its first
+                                      score-ready signal, so the bounded waits run out and
+                                      the call reports ULY_ERR_TIMEOUT */
 
 typedef struct uly_config {
   int64_t seq_len;        /* S, tokens over all ranks; S % P == 0 */

@@ -75,6 +75,7 @@ struct BwdArgs {
   float scale, scale_log2, log2_scale;
   int* status;
   uint64_t limit_ns;
+  uint32_t flags;
 };
 
 __device__ __forceinline__ void red_add4(float* addr, float x, float y, float z, float w) {
@@ -234,6 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dK_mn = sdesc_sw128(smem_u32(smem + L::kK), kBox, 1024);
       // S^T of item it over region X's S^T columns, which held dQ^T(it-2) until the
       // element-wise warps read it out (dq_free).
+      // ULY_FLAG_INJECT_STALL: block 0 withholds S^T(0)'s commit, so the element-wise
+      // warps' bounded wait for it runs out (failure-path test; nothing faults).
+      const bool stall = (a.flags & ULY_FLAG_INJECT_STALL) && blockIdx.x == 0;
       auto mma_s = [&](int it) -> bool {
         const int X = it & 1, st = it % NST;
         if (!mbar_wait(&qd_full[st], (it / NST) & 1, wc)) return false;
@@ -246,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t offb = ((kk / 4) * kBox64 + (kk % 4) * 32) >> 4;
           mma_ss(tbase + 128 * X, dK_k + offa, dQ_k + offb, id_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[X]);
+        if (!(stall && it == 0)) mma_commit(&s_full[X]);
         return true;
       };
       // dQ^T of item it over region X's S^T columns
@@ -626,6 +630,7 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   a.log2_scale = log2f(p.scale);
   a.status = p.status;
   a.limit_ns = p.limit_ns;
+  a.flags = p.cfg.flags;
   cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        BwdLayout<D>::kBytes);

@@ -1,5 +1,6 @@
-"""Failure detection without a GPU fault: a plan flag makes the forward kernel's MMA
-issuer withhold one completion signal, so the softmax warps' bounded waits run out.
+"""Failure detection without a GPU fault: a plan flag makes the forward (or backward)
+kernel's MMA issuer withhold one completion signal, so the element-wise warps' bounded
+waits run out.
 The kernel must end on its own, report ULY_ERR_TIMEOUT through the plan's status word,
 and leave the CUDA context usable for the next plan."""
 import numpy as np
@@ -39,3 +40,40 @@ def test_stalled_wait_times_out_and_context_survives():
     ro, rl = O.ulysses_attention(*(synthetic.bf16_to_f64(a) for a in (q, k, v)))
     assert_close(host_f64(o), ro, "o after a timed-out launch")
     assert_close(host_f64(lse), rl, "lse after a timed-out launch")
+
+
+def test_stalled_backward_times_out_and_context_survives():
+    """The backward's S^T issuer withholds its first commit in block 0: every wait in the
+    kernel is bounded, so the call ends, reports ULY_ERR_TIMEOUT, and a fresh plan then
+    gives oracle-correct gradients."""
+    S, P, H, G, D = 1024, 2, 4, 2, 128
+    good = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
+    q = synthetic.normal_bf16(0, synthetic.TENSOR_Q, (P, S, H // P, D))
+    k = synthetic.normal_bf16(0, synthetic.TENSOR_K, (P, S, G // P, D))
+    v = synthetic.normal_bf16(0, synthetic.TENSOR_V, (P, S, G // P, D))
+    do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D))
+    qg, kg, vg, dog = (dev_bf16(a) for a in (q, k, v, do))
+    o, o_lo = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, H // P, D))
+    lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
+    U.ulysses_attn_fwd(good, qg, kg, vg, o, lse, o_lo=o_lo)
+    assert U.ulysses_sync_status(good) == U.ULY_OK
+
+    def bwd(plan):
+        ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device="cuda")
+        dq, dk, dv = empty_bf16(q.shape), empty_bf16(k.shape), empty_bf16(v.shape)
+        U.ulysses_attn_bwd(plan, qg, kg, vg, o, lse, dog, dq, dk, dv, ws, o_lo=o_lo)
+        return dq, dk, dv
+
+    bad = U.ulysses_plan(U.make_config(S, P, 64, H, G, D, flags=U.ULY_FLAG_INJECT_STALL,
+                                       wait_timeout_ms=100))
+    bwd(bad)
+    assert U.ulysses_sync_status(bad) == U.ULY_ERR_TIMEOUT
+    bad.close()
+    dq, dk, dv = bwd(good)
+    assert U.ulysses_sync_status(good) == U.ULY_OK
+    qf, kf, vf, dof = (synthetic.bf16_to_f64(a) for a in (q, k, v, do))
+    for r in range(P):
+        rdq, rdk, rdv = O.causal_attention_bwd(qf[r], kf[r], vf[r], dof[r])
+        assert_close(host_f64(dq)[r], rdq, "dq after a timed-out backward")
+        assert_close(host_f64(dk)[r], rdk, "dk after a timed-out backward")
+        assert_close(host_f64(dv)[r], rdv, "dv after a timed-out backward")
