@@ -44,10 +44,10 @@ def attn_flops(S, H, D):
 # (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none).
 # Valid only for the kernel source it was taken on: the figure is dropped (null) as soon as
 # the hash of that source changes.
-BWD_TRAFFIC = {"bytes": (4.30 + 4.26 + (0.26845 + 0.21484) + (0.26851 + 0.21321) + 17.28 + 8.81
+BWD_TRAFFIC = {"bytes": (4.30 + 4.26 + (0.26847 + 0.21473) + (0.26849 + 0.21394) + 17.60 + 8.94
                          + 2.15 + 1.04) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "8659c4f2aebc230383f46af7f0fc9951683a97c6552d8b2fcf88ee2fd28e83a4"}
+               "source_sha256": "491f8e69edc769288d18475f1c606720dbecc88e1b462a9bd5c97b62209f99fc"}
 
 
 def bwd_traffic(seq_len):
