@@ -26,7 +26,9 @@ def _ok(plan):
 
 
 PERMUTE_CASES = [(1024, 4, 8, 8, 64), (2048, 8, 32, 8, 128), (1000, 4, 8, 4, 128),
-                 (8, 8, 8, 8, 64), (24, 1, 4, 2, 64), (4096, 2, 4, 2, 128)]
+                 (8, 8, 8, 8, 64), (24, 1, 4, 2, 64), (4096, 2, 4, 2, 128),
+                 (4096, 16, 32, 16, 128),   # 16 ranks, one KV head each
+                 (2048, 4, 32, 4, 128)]     # GQA 8:1
 
 
 @pytest.mark.parametrize("S,P,H,G,D", PERMUTE_CASES)
@@ -127,6 +129,8 @@ ATTN_CASES = [  # S, P, H, G, D, std of q/k/v
     (384, 2, 4, 2, 64, 1.0),         # odd number of 128-row tiles
     (130, 1, 2, 1, 128, 1.0),        # one rank, tail of 2 rows
     (8, 8, 8, 8, 64, 1.0),           # one token per rank
+    (4096, 16, 32, 16, 128, 1.0),    # 16 ranks: two query heads and one KV head per rank
+    (2048, 4, 32, 4, 128, 1.28),     # GQA 8:1
 ]
 
 

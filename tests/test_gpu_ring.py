@@ -47,6 +47,8 @@ RING_CASES = [  # S, P, H, G, D, std
     (384, 2, 4, 2, 64, 1.0),
     (8, 8, 8, 8, 64, 1.0),           # one token per rank
     (130, 1, 2, 1, 128, 1.0),        # one rank: the diagonal step only
+    (4096, 16, 32, 16, 128, 1.0),    # 16 ranks, 15 shard rotations
+    (2048, 4, 32, 4, 128, 1.28),     # GQA 8:1
 ]
 
 
