@@ -248,14 +248,18 @@ def run_ours(args):
     # fp16 copies, main, dQ conversion), head_to_seq of the gradients
     launches_per_step = 1 + 1 + 1 + 1 + 1 + 5 + 1
 
-    def step(ev=None, io=None):
+    def step(ev=None, io=None, sync=None):
         # io: the step's input and output buffers (x, dO_seq, o_seq, dqkv_seq)
+        # sync (end-to-end runs): events the step waits for before it first reads x and dO,
+        # and records once o_seq is final
         xs, dos, os_, dqs = io if io is not None else (x, do_seq, o_seq, dqkv_seq)
 
         def mark(i):
             if ev is not None:
                 ev[i].record(stream)
         mark(0)
+        if sync is not None:
+            stream.wait_event(sync["x"])
         U.ulysses_qkv_proj(plan, xs, wq, qkv, sid)
         mark(1)
         U.ulysses_seq_to_head(plan, qkv, q, k, v, apply_rope=True, stream=sid)
@@ -263,7 +267,11 @@ def run_ours(args):
         U.ulysses_attn_fwd(plan, q, k, v, o, lse, sid, o_lo=o_lo)
         mark(3)
         U.ulysses_head_to_seq(plan, o, H, os_, sid)
+        if sync is not None:
+            sync["o"].record(stream)
         mark(4)
+        if sync is not None:
+            stream.wait_event(sync["do"])
         U.ulysses_seq_to_head_heads(plan, dos, H, do, sid)
         mark(5)
         U.ulysses_attn_bwd(plan, q, k, v, o, lse, do, dq, dk, dv, ws, sid, o_lo=o_lo)
@@ -339,10 +347,15 @@ def run_ours(args):
         up = torch.cuda.Stream(dev)      # host -> device
         down = torch.cuda.Stream(dev)    # device -> host
         ev = lambda: torch.cuda.Event()   # noqa: E731
-        uploaded = [ev(), ev()]     # inputs of set b are on the device
+        x_up = [ev(), ev()]         # x of set b is on the device
+        do_up = [ev(), ev()]        # dO of set b is on the device
+        o_ready = [ev(), ev()]      # o_seq of set b is final
         computed = [ev(), ev()]     # the step on set b is done (inputs free, outputs ready)
         read_back = [ev(), ev()]    # outputs of set b are on the host
 
+        # x is uploaded first and dO after it: the step reads dO only at its backward half,
+        # and o_seq goes back to the host as soon as it is final, so only the first step's x
+        # and the last step's dqkv_seq cannot overlap compute.
         def e2e_run(n):
             for i in range(n):
                 b = i % 2
@@ -351,16 +364,17 @@ def run_ours(args):
                     if i >= 2:
                         up.wait_event(computed[b])
                     xs.copy_(hx, non_blocking=True)
+                    x_up[b].record(up)
                     dos.copy_(hdo, non_blocking=True)
-                    uploaded[b].record(up)
-                stream.wait_event(uploaded[b])
+                    do_up[b].record(up)
                 if i >= 2:
                     stream.wait_event(read_back[b])
-                step(io=sets[b])
+                step(io=sets[b], sync={"x": x_up[b], "do": do_up[b], "o": o_ready[b]})
                 computed[b].record(stream)
                 with torch.cuda.stream(down):
-                    down.wait_event(computed[b])
+                    down.wait_event(o_ready[b])
                     houts[b][0].copy_(os_, non_blocking=True)
+                    down.wait_event(computed[b])
                     houts[b][1].copy_(dqs, non_blocking=True)
                     read_back[b].record(down)
             for b in range(min(n, 2)):
