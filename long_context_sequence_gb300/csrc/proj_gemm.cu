@@ -168,7 +168,16 @@ __global__ void __launch_bounds__(128, 1)
       uint32_t r[32];
       tmem_ld32(tbase + ((uint32_t)(warp * 32) << 16) + c * 32, r);
       const int gn = n0 + c * 32;
-      if (gm < M && gn < N) {
+      if (OUT_F32 && out_split < 0) {
+        // transposed fp32 output out[n][m]: for each column the warp's 32 rows are 32
+        // consecutive floats (one 128-byte store)
+        if (gm < M) {
+          float* ocol = static_cast<float*>(out) + gm;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (gn + j < N) ocol[(size_t)(gn + j) * M] = __uint_as_float(r[j]);
+        }
+      } else if (gm < M && gn < N) {
         // row-major [M][N], or the head layout [N/split][M][split] (32-column chunks never
         // straddle two parts since split is a multiple of 64)
         const size_t row_off = out_split ? ((size_t)(gn / out_split) * M + gm) * out_split +
@@ -228,8 +237,8 @@ inline Operand plain(const void* base, uint64_t cols, uint64_t rows) {
   return Operand{base, cols, rows, 1};
 }
 
-// out[M][N] = sum_k A(m, k) B(n, k).  out_split = 0: out is row-major [M][N]; else it is the
-// head layout [N / out_split][M][out_split].
+// out[M][N] = sum_k A(m, k) B(n, k).  out_split = 0: out is row-major [M][N]; > 0: the head
+// layout [N / out_split][M][out_split]; < 0 (fp32 only): transposed, out[n][m].
 template <bool A_MN, bool B_MN, bool OUT_F32>
 cudaError_t run_gemm(const Plan& p, Operand a, Operand b, void* out, int M, int N, int K,
                      int out_split, cudaStream_t st) {
@@ -297,9 +306,10 @@ cudaError_t launch_o_proj_bwd(const Plan& p, const void* o_head, const void* wo,
     if (e != cudaSuccess) return e;
   }
   if (dwo) {
-    // dwo[j][c] = sum_s dy[s][j] o(s, c)
-    const Operand b{o_head, (uint64_t)part, (uint64_t)S, (uint64_t)p.P};
-    cudaError_t e = run_gemm<true, true, true>(p, plain(dy, Hd, S), b, dwo, Hd, HD, S, 0, st);
+    // dwo[j][c] = sum_s dy[s][j] o(s, c), computed as its transpose (m = c, n = j) so that
+    // the head-layout operand is A (two boxes per stage) and dy is B; stored transposed
+    const Operand a{o_head, (uint64_t)part, (uint64_t)S, (uint64_t)p.P};
+    cudaError_t e = run_gemm<true, true, true>(p, a, plain(dy, Hd, S), dwo, HD, Hd, S, -1, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
