@@ -30,7 +30,8 @@
 // o_proj:      A = o (head layout, K-major), B = wo [hidden][H*D] (K-major), out bf16 [S][hidden]
 // d(o):        A = dy [S][hidden] (K-major), B(n=c, k=j) = wo[j][c] (MN-major), out bf16 in
 //              the head layout
-// dwo:         A(m=j, k=s) = dy[s][j] (MN-major), B(n=c, k=s) = o (head layout, MN-major), fp32
+// dwo^T:       A(m=c, k=s) = o (head layout, MN-major), B(n=j, k=s) = dy[s][j] (MN-major),
+//              fp32 stored transposed (dwo[j][c])
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
