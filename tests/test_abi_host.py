@@ -83,3 +83,31 @@ def test_null_plan_is_rejected(lib):
 def test_ring_volume_matches_oracle_closed_form(lib, S, P, H, G, D):
     assert U.ulysses_ring_volume(U.make_config(S, P, 4096, H, G, D)) == \
         O.ring_volume_bytes(S, P, G, D)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """Without libulysses.so every entry point raises: there is no CPU or PyTorch fallback
+    behind the binding.  (A fresh interpreter, so that this session's loaded library is not
+    reused.)"""
+    import subprocess
+    import sys
+    code = (
+        "import functools\n"
+        "import long_context_sequence_gb300 as U\n"
+        "U.load_library = functools.partial(U.load_library, %r)\n"
+        "failures = 0\n"
+        "for call in (lambda: U.ulysses_plan(U.make_config(1024, 4, 512, 8, 8, 64)),\n"
+        "             lambda: U.ulysses_last_error(),\n"
+        "             lambda: U.ulysses_a2a_volume(U.make_config(1024, 4, 512, 8, 8, 64))):\n"
+        "    try:\n"
+        "        call()\n"
+        "    except ImportError as e:\n"
+        "        assert 'not built' in str(e)\n"
+        "        failures += 1\n"
+        "print(failures)\n"
+    ) % str(tmp_path / "missing.so")
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    out = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         cwd=ROOT, timeout=120)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "3"
