@@ -83,6 +83,12 @@ def test_backward_8b_block_64k_sampled_rows():
     _bwd_check(65536, 8, H8B, G8B, D8B, STD8B, 256, 256, "S=64K")
 
 
+def test_backward_8b_block_128k_sampled_rows():
+    """The benchmarked workload itself, S=131072, P=8: dQ on sampled rows, dK/dV on the last
+    256 keys, three ranks checked."""
+    _bwd_check(131072, 8, H8B, G8B, D8B, STD8B, 128, 256, "S=128K")
+
+
 def test_million_token_head_group_fwd_bwd():
     """One rank's post-all-to-all share at S = 2^20: 4 query heads, 1 KV head, D=128,
     Q/K/V ~ N(0,1) (a rotation of iid normals is again iid normal, so RoPE does not change
