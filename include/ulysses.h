@@ -100,8 +100,8 @@ uly_status ulysses_plan_destroy(uly_plan plan);
  * 256-byte aligned. */
 size_t ulysses_workspace_bytes(uly_plan plan);
 
-/* Local QKV projection of every shard ("each rank computes its local QKV projection",
- * Ulysses-trick page para 2): qkv[s][c] = sum_k x[s][k] * w[c][k], fp32 accumulation,
+/* Local QKV projection of every shard (Ulysses-trick page para 2: the projection happens
+ * on each rank before any exchange): qkv[s][c] = sum_k x[s][k] * w[c][k], fp32 accumulation,
  * bf16 round-to-nearest-even output.  x [S][hidden], w [C][hidden], qkv [S][C] = the
  * qkv_seq layout.  All ranks share w, so this is one GEMM over all S rows. */
 uly_status ulysses_qkv_proj(uly_plan plan, const void *x, const void *w, void *qkv,
@@ -121,9 +121,9 @@ uly_status ulysses_seq_to_head(uly_plan plan, const void *qkv_seq, int in_fp32,
 uly_status ulysses_seq_to_head_heads(uly_plan plan, const void *x_seq, int n_heads,
                                      void *x_head, void *stream);
 
-/* Causal GQA attention of every rank's head group over the full sequence ("each GPU can
- * compute its share using standard FlashAttention locally", Ulysses-trick page para 2;
- * tiled so no S x S matrix is ever stored, Hugging Face post para 3).  For query head
+/* Causal GQA attention of every rank's head group over the full sequence (Ulysses-trick
+ * page para 2: heads do not interact, so a rank runs ordinary flash attention on the heads
+ * it holds; tiled so no S x S matrix is ever stored, Hugging Face post para 3).  For query head
  * h' of rank r (KV head h' / (H/G)):  o = softmax(scale * q k^T, causal) v in bf16 with
  * fp32 softmax and accumulation; lse = natural-log logsumexp of the scaled scores.
  * o_lo (optional, may be NULL; layout of o): receives bf16(O - o), what the bf16 rounding
@@ -160,8 +160,8 @@ uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void *q, const void *k,
                                     const float *lse, const void *d_o, void *dq, void *dk,
                                     void *dv, void *stream);
 
-/* head->seq all-to-all, the inverse of seq->head ("another all-to-all operation reverses
- * the redistribution", Hugging Face post para 5): x_head [P][S][n_heads/P][D] ->
+/* head->seq all-to-all, the inverse of seq->head (Hugging Face post para 5: a second
+ * exchange undoes the first and brings back the sequence sharding): x_head [P][S][n_heads/P][D] ->
  * x_seq [P][S/P][n_heads][D].  n_heads = H for o and dq, G for dk and dv. */
 uly_status ulysses_head_to_seq(uly_plan plan, const void *x_head, int n_heads, void *x_seq,
                                void *stream);
