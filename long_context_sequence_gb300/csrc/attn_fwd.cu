@@ -1,8 +1,8 @@
 // Causal GQA attention forward of every virtual rank's head group, with logsumexp.
 //
 // "Snowflake's Ulysses trick ..." para 2: after the seq->head all-to-all each rank holds
-// the full sequence for its heads, and "since attention heads are independent" runs
-// FlashAttention on them locally.  "Ulysses Sequence Parallelism: Training with
+// the full sequence for its heads and, heads not interacting, runs flash attention on
+// them on its own.  "Ulysses Sequence Parallelism: Training with
 // Million-Token Contexts" para 3: tiling never materialises the S x S score matrix.
 //
 // Design (sm_103a, tcgen05):
