@@ -83,6 +83,20 @@ def test_backward_8b_block_64k_sampled_rows():
     _bwd_check(65536, 8, H8B, G8B, D8B, STD8B, 256, 256, "S=64K")
 
 
+def test_head_dim_64_fwd_bwd_32k_sampled_rows():
+    """D = 64 kernels at size: S=32768, P=4, 16 query heads and 4 KV heads (GQA 4:1), std
+    0.45; forward on sampled rows of every rank, backward on sampled dQ rows and tail keys."""
+    S, P, H, G, D, std = 32768, 4, 16, 4, 64, 0.45
+    plan = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
+    q, k, v = _gen(S, P, H, G, D, std)
+    o = empty_bf16((P, S, H // P, D))
+    lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
+    U.ulysses_attn_fwd(plan, dev_bf16(q), dev_bf16(k), dev_bf16(v), o, lse)
+    assert U.ulysses_sync_status(plan) == U.ULY_OK, U.ulysses_last_error()
+    _check_fwd_rows(q, k, v, o, lse, synthetic.sample_rows(S, P, 128), P, H, G, "D=64")
+    _bwd_check(S, P, H, G, D, std, 128, 256, "D=64")
+
+
 def test_backward_8b_block_128k_sampled_rows():
     """The benchmarked workload itself, S=131072, P=8: dQ on sampled rows, dK/dV on the last
     256 keys, three ranks checked."""
