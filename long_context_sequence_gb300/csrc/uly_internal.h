@@ -41,11 +41,13 @@ cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk
                                    const void* dv, bool rope, void* out, cudaStream_t st);
 cudaError_t launch_qkv_gemm(const Plan& p, const void* x, const void* w, void* out,
                             cudaStream_t st);
-// dx = dqkv w (bf16 [S][hidden]) and dw = dqkv^T x (fp32 [C][hidden]); either may be null.
+// y = o wo^T with o read in the head layout (bf16 [S][hidden]).
 cudaError_t launch_o_proj(const Plan& p, const void* o_head, const void* wo, void* y,
                           cudaStream_t st);
+// dO = dy wo written in the head layout and dwo = dy^T o (fp32 [hidden][H*D]).
 cudaError_t launch_o_proj_bwd(const Plan& p, const void* o_head, const void* wo, const void* dy,
                               void* do_head, float* dwo, cudaStream_t st);
+// dx = dqkv w (bf16 [S][hidden]) and dw = dqkv^T x (fp32 [C][hidden]); either may be null.
 cudaError_t launch_qkv_gemm_bwd(const Plan& p, const void* x, const void* w, const void* dqkv,
                                 void* dx, float* dw, cudaStream_t st);
 cudaError_t launch_attn_fwd(const Plan& p, const void* q, const void* k, const void* v,
