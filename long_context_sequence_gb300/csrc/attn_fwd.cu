@@ -10,8 +10,14 @@
 //     that share every K/V tile; blocks are issued heaviest (longest causal prefix) first
 //     and neighbouring blocks are the query heads of one KV head, so K/V stay in L2;
 //   * warp 8 (TMA): Q0/Q1 once, then K_j and V_j into a 2-deep ring (128-byte swizzle);
-//   * warp 9 (MMA, one thread): S_t = Q_t K_j^T into TMEM (fp32, 128 columns each), then
-//     O_t += P_t V_j with P_t read from TMEM (bf16, written over S_t);
+//   * warps 9 and 10 (MMA, one thread each, one per query tile t): S_t = Q_t K_j^T into
+//     TMEM (fp32, 128 columns), then O_t += P_t V_j with P_t read from TMEM (bf16, written
+//     over S_t; the same thread issues P_t V_j before the next S_t, so in order).  The two
+//     threads take turns, unit by unit, in the order P_0 V_{j-1}, S_0(j), P_1 V_{j-1},
+//     S_1(j), ...: so one tile's softmax runs while the tensor core works on the other
+//     tile.  One thread spends ~60 cycles issuing a tcgen05.mma and ~150 on a commit,
+//     against the tensor core's 64 cycles for a 128 x 128 x 16 step; with two threads the
+//     barrier waits and commits of one overlap the other's issue.  Both release K/V slots;
 //   * warps 0-3 / 4-7: the online softmax of Q0 / Q1, one thread per row (= TMEM lane),
 //     in the log2 domain, with lazy rescaling of O (only when the running max grows by
 //     more than 2^8); they also write O / l (bf16), optionally its bf16 rounding residual
@@ -35,8 +41,8 @@ namespace uly {
 namespace {
 
 constexpr int BM = 128, BN = 128;
-constexpr int kThreads = 320;
-constexpr int kTmaWarp = 8, kMmaWarp = 9;
+constexpr int kThreads = 352;
+constexpr int kTmaWarp = 8, kMmaWarp = 9;   // MMA warps 9 (tile 0) and 10 (tile 1)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kBox = 128 * 64 * 2;   // one [128 rows][64 elements] bf16 box
 
@@ -89,9 +95,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = bars + 9;    // [2] one per query tile
   uint64_t* p_full = bars + 11;   // [2]
   uint64_t* o_done = bars + 13;   // [2]
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* drain = bars + 15;    // [2] one per MMA thread
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+  volatile int* units_done = abort_flag + 1;   // [2] issue units each MMA thread has issued
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -111,16 +118,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    units_done[0] = units_done[1] = 0;
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_empty[i], 1);
+      mbar_init(&k_empty[i], 2);   // both MMA threads release a K / V slot
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_empty[i], 1);
+      mbar_init(&v_empty[i], 2);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 128);
       mbar_init(&o_done[i], 1);
+      mbar_init(&drain[i], 1);
     }
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -168,18 +176,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = v_issued > 2 ? v_issued - 2 : 0; j < v_issued; ++j)
         mbar_drain(&v_full[j & 1], (j >> 1) & 1, a.limit_ns);
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
     if (lane == 0) {
+      const int t = warp - kMmaWarp;   // this thread's query tile
+      const int nt = t ? n1 : n0;      // its KV steps; tile 1 may take one more than tile 0
       constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
       constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
-      const bool stall = (a.flags & ULY_FLAG_INJECT_STALL) && blockIdx.x == 0;
+      // ULY_FLAG_INJECT_STALL: block 0 withholds S_0's first commit, so the softmax warps'
+      // bounded wait for it runs out (failure-path test; nothing faults).
+      const bool stall = (a.flags & ULY_FLAG_INJECT_STALL) && blockIdx.x == 0 && t == 0;
       bool alive = mbar_wait(q_full, 0, wc);
       // descriptors built once; K-steps add byte offset / 16 (smem addresses < 2^18)
-      const uint64_t dq0 = sdesc_sw128(smem_u32(smem + L::kQ), 16, 1024);
+      const uint64_t qa = sdesc_sw128(smem_u32(smem + L::kQ + t * L::kTile), 16, 1024);
       const uint64_t dk0 = sdesc_sw128(smem_u32(smem + L::kK), 16, 1024);
       const uint64_t dv0 = sdesc_sw128(smem_u32(smem + L::kV), kBox, 1024);
-      auto issue_s = [&](int t, int j) {
-        const uint64_t qa = dq0 + ((t * L::kTile) >> 4);
+      auto issue_s = [&](int j) {
         const uint64_t kb = dk0 + (((j & 1) * L::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -187,45 +198,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tbase + t * BN, qa + off, kb + off, idesc_qk, kk > 0 ? 1u : 0u);
         }
       };
-      auto issue_pv = [&](int t, int j) -> bool {
-        if (!mbar_wait(&p_full[t], j & 1, wc)) return false;
-        if (!mbar_wait(&v_full[j & 1], (j >> 1) & 1, wc)) return false;
-        tc_fence_after();
+      auto issue_pv = [&](int j) {
         const uint64_t vb = dv0 + (((j & 1) * L::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ts(tbase + 2 * BN + t * D, tbase + t * BN + kk * 8, vb + ((kk * 16 * 128) >> 4),
                  idesc_pv, (j > 0 || kk > 0 || full_blk) ? 1u : 0u);
-        return true;
       };
-      for (int j = 0; alive && j < n1; ++j) {
-        if (!mbar_wait(&k_full[j & 1], (j >> 1) & 1, wc)) { alive = false; break; }
-        tc_fence_after();
-        for (int t = 0; t < 2 && alive; ++t) {
-          const int nt = t ? n1 : n0;
-          if (j < nt) {
-            if (j >= 1 && !issue_pv(t, j - 1)) { alive = false; break; }
-            issue_s(t, j);
-            if (!(stall && j == 0 && t == 0)) mma_commit(&s_full[t]);
-          } else if (j == nt) {
-            if (!issue_pv(t, j - 1)) { alive = false; break; }
-            mma_commit(&o_done[t]);
+      // Waits (bounded) until the other thread has issued `need` units.
+      auto wait_turn = [&](int need) -> bool {
+        if (units_done[1 - t] >= need) return true;
+        const uint64_t t0 = globaltimer_ns();
+        while (units_done[1 - t] < need) {
+          if (*wc.abort) return false;
+          if (globaltimer_ns() - t0 > wc.limit_ns) {
+            atomicCAS(wc.status, kOk, kErrTimeout);
+            *wc.abort = 1;
+            return false;
           }
         }
-        if (!alive) break;
-        mma_commit(&k_empty[j & 1]);
-        if (j >= 1) mma_commit(&v_empty[(j - 1) & 1]);
-      }
-      for (int t = 0; t < 2 && alive; ++t) {
-        const int nt = t ? n1 : n0;
-        if (nt == n1) {
-          if (!issue_pv(t, n1 - 1)) { alive = false; break; }
+        return true;
+      };
+      // Unit u: P_t V_{u-1} (u >= 1), then S_t(u) = Q_t K_u^T over the columns P_t held
+      // (u < nt).  Tile 0 takes its unit u after tile 1's unit u-1; tile 1 its unit u
+      // after tile 0's unit u (or after tile 0's last unit: tile 1 may take one more step).
+      // K/V slots of a step only tile 1 takes get one release; no later load waits on them.
+      for (int u = 0; alive && u <= nt; ++u) {
+        if (u >= 1) {
+          if (!mbar_wait(&p_full[t], (u - 1) & 1, wc) ||
+              !mbar_wait(&v_full[(u - 1) & 1], ((u - 1) >> 1) & 1, wc)) { alive = false; break; }
+        }
+        if (u < nt && !mbar_wait(&k_full[u & 1], (u >> 1) & 1, wc)) { alive = false; break; }
+        if (!wait_turn(t == 0 ? u : min(u + 1, n0 + 1))) { alive = false; break; }
+        tc_fence_after();
+        if (u >= 1) issue_pv(u - 1);
+        if (u < nt) issue_s(u);
+        units_done[t] = u + 1;
+        if (u < nt) {
+          if (!(stall && u == 0)) mma_commit(&s_full[t]);
+        } else {
           mma_commit(&o_done[t]);
         }
+        if (u >= 1) mma_commit(&v_empty[(u - 1) & 1]);
+        if (u < nt) mma_commit(&k_empty[u & 1]);
       }
       // All issued MMAs complete before TMEM can be freed.
-      mma_commit(drain);
-      mbar_drain(drain, 0, a.limit_ns);
+      mma_commit(&drain[t]);
+      mbar_drain(&drain[t], 0, a.limit_ns);
     }
   } else {
     // Softmax warpgroups: t = query tile, one thread per row / TMEM lane.
