@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 2);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 128);
+      mbar_init(&p_full[i], 4);    // one arrival per softmax warp
       mbar_init(&o_done[i], 1);
       mbar_init(&drain[i], 1);
     }
@@ -288,8 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       uint32_t s[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(ts + 32 * c, s[c]);
+      tmem_ld128(ts, s);
       const int kbase = j * BN;
       if ((!full_blk && kbase + BN - 1 > m0 + t * BM) || kbase + BN > a.S) {
 #pragma unroll
@@ -354,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&p_full[t]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[t]);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&o_done[t], 0, wc));
     if (ok && kRing && a.ring_t != r) {
