@@ -114,6 +114,41 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&r)[4][32])
       : "memory");
 }
 
+// Non-blocking test of a barrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 P, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, P;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_wait, but polls without suspending the thread, so it resumes as soon as the phase
+// completes.  For the single MMA-issuing threads, whose wake-up is on the critical path.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_test(bar, parity)) return true;
+    if (*w.abort) return false;
+    if (*reinterpret_cast<volatile int*>(w.status) != kOk) {   // another CTA gave up
+      *w.abort = 1;
+      return false;
+    }
+    if (globaltimer_ns() - t0 > w.limit_ns) {
+      atomicCAS(w.status, kOk, kErrTimeout);
+      *w.abort = 1;
+      __threadfence_block();
+      return false;
+    }
+  }
+}
+
 template <int D, bool kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -261,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // K/V slots of a step only tile 1 takes get one release; no later load waits on them.
       for (int u = 0; alive && u <= nt; ++u) {
         if (u >= 1) {
-          if (!mbar_wait(&p_full[t], (u - 1) & 1, wc) ||
+          if (!mbar_wait_spin(&p_full[t], (u - 1) & 1, wc) ||
               !mbar_wait(&v_full[(u - 1) & 1], ((u - 1) >> 1) & 1, wc)) { alive = false; break; }
         }
         if (u < nt && !mbar_wait(&k_full[u & 1], (u >> 1) & 1, wc)) { alive = false; break; }
