@@ -466,9 +466,10 @@ def run_ours(args):
                  "qkv_proj_bwd_tflops": 2 * proj_f / (lper["qkv_proj_bwd"] * 1e-3) / 1e12,
                  "launches_per_step": 1 + 1 + 1 + 1 + 2 + 5 + 1 + 2}
 
-    # Ring attention (the pages' comparator) on the same virtual ranks and tokens: its
-    # forward with the K/V exchange, beside the Ulysses forward path (seq->head, attention,
-    # head->seq of O), and the per-rank volumes of the two exchanges.
+    # Ring attention (what "Snowflake's Ulysses trick ..." para 3 compares Ulysses with) on
+    # the same virtual ranks and tokens: its forward with the K/V exchange, beside the
+    # Ulysses forward path (seq->head, attention, head->seq of O), and the per-rank volumes
+    # of the two exchanges.
     ring = None
     if not args.no_ring:
         n = S // P

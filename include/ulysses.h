@@ -166,8 +166,9 @@ uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void *q, const void *k,
 uly_status ulysses_head_to_seq(uly_plan plan, const void *x_head, int n_heads, void *x_seq,
                                void *stream);
 
-/* Rest of the block's training step (the pages' method is for training, Hugging Face post
- * para 1; these gradients mirror the forward steps above in reverse).
+/* Rest of the block's training step (the method is for training: "Ulysses Sequence
+ * Parallelism: Training with Million-Token Contexts" para 1; these gradients mirror the
+ * forward steps above in reverse).
  *
  * head->seq all-to-all of the attention gradients back into the projection layout:
  * dq [P][S][H/P][D], dk, dv [P][S][G/P][D] -> dqkv_seq [P][S/P][H + 2G][D] (= [S][C]),

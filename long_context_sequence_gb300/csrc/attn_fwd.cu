@@ -17,7 +17,8 @@
 //     S_1(j), ...: so one tile's softmax runs while the tensor core works on the other
 //     tile.  One thread spends ~60 cycles issuing a tcgen05.mma and ~150 on a commit,
 //     against the tensor core's 64 cycles for a 128 x 128 x 16 step; with two threads the
-//     barrier waits and commits of one overlap the other's issue.  Both release K/V slots;
+//     barrier waits and commits of one overlap the other's issue.  They poll for P without
+//     suspending, so they resume as soon as the softmax is done.  Both release K/V slots;
 //   * warps 0-3 / 4-7: the online softmax of Q0 / Q1, one thread per row (= TMEM lane),
 //     in the log2 domain, with lazy rescaling of O (only when the running max grows by
 //     more than 2^8); they also write O / l (bf16), optionally its bf16 rounding residual
@@ -25,8 +26,8 @@
 //   * causal tile skipping: Q0 sees KV tiles 0..m0/128, Q1 one more.
 // TMEM: S0 [0,128), S1 [128,256), O0 [256, 256+D), O1 [256+D, 256+2D) of 512 columns.
 //
-// The same kernel, instantiated with kRing, runs one step of ring attention (the pages'
-// comparator, "Snowflake's Ulysses trick ..." para 3) on the virtual ranks: the sequence
+// The same kernel, instantiated with kRing, runs one step of ring attention (the method
+// "Snowflake's Ulysses trick ..." para 3 compares against) on the virtual ranks: the sequence
 // stays sharded, rank r holds its queries [S/P][H][D] and, in step t, the K/V shard
 // r - t (ranks r < t hold shards after theirs, which the causal mask hides entirely, and
 // do not run).  Step 0 is the causal diagonal block; later steps are full blocks.  The
