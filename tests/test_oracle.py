@@ -104,14 +104,15 @@ def test_a2a_volume_counts_cross_rank_blocks():
 
 
 # ------------------------------------------------------------------------ projection
-def test_projection_brute_force_and_identity():
-    x = _rng(3).standard_normal((5, 4))
-    w = _rng(4).standard_normal((6, 4))
+@pytest.mark.parametrize("T,K,C", [(5, 4, 6), (4, 4, 4)])   # square: a transposed w keeps its shape
+def test_projection_brute_force_and_identity(T, K, C):
+    x = _rng(3).standard_normal((T, K))
+    w = _rng(4).standard_normal((C, K))
     y = O.qkv_projection(x, w)
-    for s in range(5):
-        for c in range(6):
-            assert abs(y[s, c] - sum(x[s, j] * w[c, j] for j in range(4))) < 1e-12
-    eye = np.eye(4)
+    for s in range(T):
+        for c in range(C):
+            assert abs(y[s, c] - sum(x[s, j] * w[c, j] for j in range(K))) < 1e-12
+    eye = np.eye(K)
     assert np.array_equal(O.qkv_projection(eye, w), w.T)
 
 
@@ -367,16 +368,17 @@ def test_rope_backward_inverts_and_matches_autograd():
     assert np.allclose(O.rope_backward(g, pos, theta), tx.grad.numpy(), rtol=0, atol=1e-12)
 
 
-def test_projection_backward_brute_force():
+@pytest.mark.parametrize("T,K,C", [(5, 4, 6), (4, 4, 4)])   # square: transposes keep their shape
+def test_projection_backward_brute_force(T, K, C):
     r = _rng(21)
-    x, w, dy = r.standard_normal((5, 4)), r.standard_normal((6, 4)), r.standard_normal((5, 6))
+    x, w, dy = r.standard_normal((T, K)), r.standard_normal((C, K)), r.standard_normal((T, C))
     dx, dw = O.qkv_projection_backward(x, w, dy)
-    for s in range(5):
-        for k in range(4):
-            assert abs(dx[s, k] - sum(dy[s, c] * w[c, k] for c in range(6))) < 1e-12
-    for c in range(6):
-        for k in range(4):
-            assert abs(dw[c, k] - sum(dy[s, c] * x[s, k] for s in range(5))) < 1e-12
+    for s in range(T):
+        for k in range(K):
+            assert abs(dx[s, k] - sum(dy[s, c] * w[c, k] for c in range(C))) < 1e-12
+    for c in range(C):
+        for k in range(K):
+            assert abs(dw[c, k] - sum(dy[s, c] * x[s, k] for s in range(T))) < 1e-12
 
 
 def test_block_backward_matches_torch_autograd():
@@ -403,12 +405,12 @@ def test_block_backward_matches_torch_autograd():
     assert np.allclose(dw, tw.grad.numpy(), rtol=0, atol=1e-10)
 
 
-def test_output_projection_brute_force():
+@pytest.mark.parametrize("T,H,D,hidden", [(5, 3, 2, 4), (4, 2, 2, 4)])   # square wo: H * D = hidden
+def test_output_projection_brute_force(T, H, D, hidden):
     """y[t][j] = sum over heads h and dims d of o[t][h][d] wo[j][h*D + d], written as loops;
     the backward the same way (do[t][h][d] = sum_j dy[t][j] wo[j][h*D+d],
     dwo[j][h*D+d] = sum_t dy[t][j] o[t][h][d])."""
     r = _rng(31)
-    T, H, D, hidden = 5, 3, 2, 4
     o, wo, dy = r.standard_normal((T, H, D)), r.standard_normal((hidden, H * D)), \
         r.standard_normal((T, hidden))
     y = O.output_projection(o, wo)
