@@ -5,6 +5,7 @@ import numpy as np
 import torch
 
 import synthetic
+from tolerances import bf16_ulp  # noqa: F401  (also used by the tests through here)
 
 MAX_ABS = 2e-2
 MEAN_ABS = 2e-3
@@ -26,11 +27,6 @@ def host_f64(t: torch.Tensor) -> np.ndarray:
 
 def empty_bf16(shape):
     return torch.empty(shape, dtype=torch.bfloat16, device="cuda")
-
-
-def bf16_ulp(x: np.ndarray) -> np.ndarray:
-    """Spacing of bf16 values at the magnitude of x (normal range)."""
-    return 2.0 ** (np.floor(np.log2(np.maximum(np.abs(x), 2.0 ** -126))) - 7)
 
 
 def assert_close(got, ref, name, max_abs=MAX_ABS, mean_abs=MEAN_ABS):

@@ -10,6 +10,7 @@ import torch
 import long_context_sequence_gb300 as U
 import oracle as O
 import synthetic
+from tolerances import assert_within as _assert_within, peaked_bounds as _peaked_bounds
 from gpu_helpers import (assert_close, bf16_ulp_distance, dev_bf16, empty_bf16, host_bits,
                          host_f64)
 
@@ -136,58 +137,6 @@ ATTN_CASES = [  # S, P, H, G, D, std of q/k/v
 
 
 PEAKED = 3.0   # q/k std at which the logits' std is ~9: a sharply peaked softmax
-
-
-def _peaked_bounds(q, k, v, do, H, G):
-    """Per-element error bounds of one rank's attention from its arithmetic, for the peaked
-    regime, where the magnitudes outgrow the absolute 2e-2 / 2e-3 bounds.  Built from the
-    fp64 quantities of the definition (P, dP, D, dS):
-      O:   P V with bf16 P (relative 2^-9 per weight) and fp32 sums: 2^-8 sum_j P_ij |v_j|;
-      dV:  fp16 P (2^-12) and fp32 sums:                     2^-11 sum_i P_ij |dO_i|;
-      dK:  fp16 dS (2^-12) and fp32 sums:            2^-11 scale sum_i |dS_ij| |q_i|;
-      dQ:  likewise                                   2^-11 scale sum_j |dS_ij| |k_j|;
-    and, through dS_ij = P_ij (dP_ij - D_i), the row term D_i = dO_i . O_i formed from O held
-    as bf16 plus its bf16 residual (relative 2^-16, fp32 dot): |dD_i| <= 2^-15 sum |dO_i O_i|,
-    adding scale |dD_i| sum_j P_ij |k_j| to dQ and scale sum_i P_ij |dD_i| |q_i| to dK;
-    and fp16's subnormal floor: the stored scale*P and scale*dS below 2^-14 round to a
-    2^-24 grid, an absolute 2^-25 each, adding 2^-25 sum over visible keys |k_j| to dQ,
-    2^-25 sum over visible queries |q_i| to dK and 2^-25 / scale sum |dO_i| to dV;
-    each plus one bf16 ulp of the value for the output's own rounding (in the check)."""
-    S, hl, D = q.shape
-    gl = k.shape[1]
-    grp = hl // gl
-    scale = 1.0 / np.sqrt(D)
-    bo, bq = np.zeros_like(q), np.zeros_like(q)
-    bk, bv = np.zeros_like(k), np.zeros_like(v)
-    mask = np.tril(np.ones((S, S), bool))
-    for h in range(hl):
-        g = h // grp
-        s = np.where(mask, scale * q[:, h] @ k[:, g].T, -np.inf)
-        p = np.exp(s - s.max(axis=1, keepdims=True))
-        p /= p.sum(axis=1, keepdims=True)
-        o = p @ v[:, g]
-        dp = do[:, h] @ v[:, g].T
-        ds = np.where(mask, p * (dp - np.sum(do[:, h] * o, axis=1, keepdims=True)), 0.0)
-        dd = 2.0 ** -15 * np.sum(np.abs(do[:, h] * o), axis=1)          # |error of D_i|
-        bo[:, h] = 2.0 ** -8 * (p @ np.abs(v[:, g]))
-        bq[:, h] = 2.0 ** -11 * scale * (np.abs(ds) @ np.abs(k[:, g])) + \
-            scale * dd[:, None] * (p @ np.abs(k[:, g]))
-        bk[:, g] += 2.0 ** -11 * scale * (np.abs(ds).T @ np.abs(q[:, h])) + \
-            scale * (p * dd[:, None]).T @ np.abs(q[:, h])
-        bv[:, g] += 2.0 ** -11 * (p.T @ np.abs(do[:, h]))
-        m = mask.astype(np.float64)
-        bq[:, h] += 2.0 ** -25 * (m @ np.abs(k[:, g]))
-        bk[:, g] += 2.0 ** -25 * (m.T @ np.abs(q[:, h]))
-        bv[:, g] += 2.0 ** -25 / scale * (m.T @ np.abs(do[:, h]))
-    return bo, bq, bk, bv
-
-
-def _assert_within(got, ref, bound, name):
-    from gpu_helpers import bf16_ulp
-    err = np.abs(np.asarray(got, np.float64) - ref)
-    lim = bound + bf16_ulp(ref)
-    worst = np.unravel_index(np.argmax(err / lim), err.shape)
-    assert np.all(err <= lim), "%s: err %.3g > bound %.3g at %s" % (name, err[worst], lim[worst], worst)
 
 
 @pytest.mark.parametrize("S,P,H,G,D,std", ATTN_CASES)

@@ -11,6 +11,7 @@ import torch
 import long_context_sequence_gb300 as U
 import oracle as O
 import synthetic
+from tolerances import assert_rel as _assert_rel
 from gpu_helpers import assert_close, dev_bf16, empty_bf16, host_bits, host_f64
 
 pytestmark = pytest.mark.gpu
@@ -108,21 +109,6 @@ def test_qkv_projection_backward(S, hidden, C):
     U.ulysses_qkv_proj_bwd(plan, dev_bf16(x), dev_bf16(w), dev_bf16(dy), None, dw2)
     _ok(plan)
     assert torch.equal(dx2, dx) and torch.equal(dw2, dw)
-
-
-def _assert_rel(got, ref, name, rel_max=2e-2, rel_norm=1.5e-2):
-    """End-to-end gradients against the unrounded fp64 pipeline, scaled to the gradient's
-    magnitude: dw is a sum over all S tokens (|dw| reaches ~100 on the 8B shape), so an
-    absolute bound does not fit it.  Storage of every intermediate in bf16 alone gives
-    max|err|/max|ref| ~ 6e-3 and a normwise error ~ 6e-3 on the 8B shape."""
-    got = np.asarray(got, np.float64)
-    ref = np.asarray(ref, np.float64)
-    assert got.shape == ref.shape and np.all(np.isfinite(got)), name
-    d = np.abs(got - ref)
-    m = np.abs(ref).max()
-    rn = np.linalg.norm(got - ref) / np.linalg.norm(ref)
-    assert d.max() <= rel_max * m and rn <= rel_norm, \
-        "%s: max|err| %.3g (max|ref| %.3g), normwise %.3g" % (name, d.max(), m, rn)
 
 
 def _training_step(S, P, hidden, H, G, D, theta):

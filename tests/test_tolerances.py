@@ -1,0 +1,127 @@
+"""The GPU tests' error bounds, checked on the CPU against the arithmetic they come from.
+
+A bound must admit a correct kernel and still catch a wrong one. So for each bound a numpy
+simulation applies to the fp64 definition exactly the roundings the kernels declare, and must
+stay inside the bound with margin. Where a plausible coarser rounding exists (bf16 where the
+kernel keeps fp16), the simulation with that rounding must leave the bound."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic
+from oracle import ulysses_oracle as OU
+from tolerances import assert_rel, bf16_ulp, peaked_bounds
+
+
+def _bf16(a):
+    return synthetic.bf16_to_f64(synthetic.f32_to_bf16(np.asarray(a, np.float32)))
+
+
+def _f16(a):
+    return np.asarray(a, np.float16).astype(np.float64)
+
+
+# ------------------------------------------------------------- peaked-softmax bounds
+def _peaked_rank0(S=1024, P=4, H=8, G=4, D=128, std=3.0):
+    """Rank 0's inputs of the GPU tests' peaked case (same generator keys)."""
+    f = lambda bits: synthetic.bf16_to_f64(bits)[0]
+    q = f(synthetic.normal_bf16(0, synthetic.TENSOR_Q, (P, S, H // P, D), std=std))
+    k = f(synthetic.normal_bf16(0, synthetic.TENSOR_K, (P, S, G // P, D), std=std))
+    v = f(synthetic.normal_bf16(0, synthetic.TENSOR_V, (P, S, G // P, D), std=std))
+    do = f(synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D)))
+    return q, k, v, do
+
+
+def _simulate(q, k, v, do, p_store, ds_store):
+    """The kernels' roundings on the fp64 definition:
+    - forward: unnormalised P (relative to the row max) stored as bf16 for P V; the row sum
+      from the unrounded P;
+    - backward: O held as bf16 plus its bf16 residual for the row term D; P_s = scale * P
+      unrounded; dS = P_s (dP - D) from the unrounded P_s, stored with `ds_store` for dQ and
+      dK; P_s stored with `p_store` for dV (divided by the scale at the end);
+    - every output rounded once to bf16."""
+    S, hl, D = q.shape
+    gl = k.shape[1]
+    grp, scale = hl // gl, 1.0 / np.sqrt(D)
+    o, lse = O.causal_attention(q, k, v)
+    o_hi = _bf16(o)
+    o_lo = _bf16(o - o_hi)
+    mask = np.tril(np.ones((S, S), bool))
+    o_sim, dq = np.zeros_like(q), np.zeros_like(q)
+    dk, dv = np.zeros_like(k), np.zeros_like(v)
+    for h in range(hl):
+        g = h // grp
+        s = np.where(mask, scale * q[:, h] @ k[:, g].T, -np.inf)
+        pu = np.exp(s - s.max(axis=1, keepdims=True))
+        o_sim[:, h] = (_bf16(pu) @ v[:, g]) / pu.sum(axis=1)[:, None]
+        d_row = np.sum(do[:, h] * (o_hi[:, h] + o_lo[:, h]), axis=1)
+        ps = np.where(mask, scale * np.exp(s - lse[h][:, None]), 0.0)
+        ds = ds_store(ps * (do[:, h] @ v[:, g].T - d_row[:, None]))
+        dq[:, h] = ds @ k[:, g]
+        dk[:, g] += ds.T @ q[:, h]
+        dv[:, g] += (p_store(ps).T @ do[:, h]) / scale
+    return tuple(_bf16(t) for t in (o_sim, dq, dk, dv))
+
+
+def _ratios(sim, ref, bounds):
+    """Worst error over bound per output, the bound widened by one bf16 ulp as in the tests."""
+    return [float((np.abs(s - r) / (b + bf16_ulp(r))).max()) for s, r, b in zip(sim, ref, bounds)]
+
+
+@pytest.fixture(scope="module")
+def peaked():
+    q, k, v, do = _peaked_rank0()
+    o, _ = O.causal_attention(q, k, v)
+    dq, dk, dv = O.causal_attention_bwd(q, k, v, do)
+    return (q, k, v, do), (o, dq, dk, dv), peaked_bounds(q, k, v, do, 8, 4)
+
+
+def test_peaked_bounds_admit_the_kernels_roundings(peaked):
+    inputs, ref, bounds = peaked
+    ratios = _ratios(_simulate(*inputs, _f16, _f16), ref, bounds)
+    assert max(ratios) <= 0.9, dict(zip(("o", "dq", "dk", "dv"), ratios))
+
+
+def test_peaked_bounds_catch_bf16_ds(peaked):
+    inputs, ref, bounds = peaked
+    _, rq, rk, _ = _ratios(_simulate(*inputs, _f16, _bf16), ref, bounds)
+    assert rq >= 1.5 and rk >= 1.5, (rq, rk)
+
+
+def test_peaked_bounds_catch_bf16_p_for_dv(peaked):
+    inputs, ref, bounds = peaked
+    rv = _ratios(_simulate(*inputs, _bf16, _f16), ref, bounds)[3]
+    assert rv >= 1.5, rv
+
+
+# ------------------------------------------------------- whole-step gradient tolerance
+@pytest.mark.parametrize("S,P,hidden,H,G,D,theta", [(1024, 4, 512, 8, 8, 64, 0.0),
+                                                    (2048, 8, 4096, 32, 8, 128, 500000.0)])
+def test_training_step_tolerance_leaves_room_beyond_bf16_storage(S, P, hidden, H, G, D, theta):
+    """The whole-step gradients (dqkv, dx, dW) are held to max|err| <= 2e-2 max|ref| and a
+    normwise error <= 1.5e-2 against the unrounded fp64 pipeline.  Storing every
+    intermediate as bf16 (projection output, RoPE'd q/k, dQ/dK/dV, the gradient after the
+    RoPE backward, dx), with everything else exact, must use at most half of that, leaving
+    the other half to the kernels' internal roundings (which the stage bounds cover)."""
+    x = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_X, (S, hidden)))
+    w = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_W, ((H + 2 * G) * D, hidden),
+                                                    std=0.02))
+    do = synthetic.bf16_to_f64(synthetic.normal_bf16(synthetic.SEED_DO, 0, (S, H, D)))
+    rdx, rdw, rdqkv = O.ulysses_block_backward(x, w, do, P, H, G, D, theta)
+    qkv = _bf16(O.qkv_projection(x, w)).reshape(S, H + 2 * G, D)
+    pos = np.arange(S)
+    if theta:
+        qkv = np.concatenate([_bf16(O.apply_rope(qkv[:, :H + G], pos, theta)), qkv[:, H + G:]],
+                             axis=1)
+    q, k, v = O.seq_to_head(qkv, P, H, G)
+    do_head = OU._seq_to_head_one(do, P)
+    grads = [O.causal_attention_bwd(q[r], k[r], v[r], do_head[r]) for r in range(P)]
+    dq, dk, dv = (np.stack([_bf16(g[i]) for g in grads]) for i in range(3))
+    g = O.head_to_seq_qkv(dq, dk, dv, P)
+    if theta:
+        g = np.concatenate([_bf16(O.rope_backward(g[:, :H + G], pos, theta)), g[:, H + G:]],
+                           axis=1)
+    g = _bf16(g)
+    dx, dw = O.qkv_projection_backward(x, w, g.reshape(S, -1))
+    for name, got, ref in (("dqkv", g, rdqkv), ("dx", _bf16(dx), rdx), ("dw", dw, rdw)):
+        assert_rel(got, ref, name, rel_max=1e-2, rel_norm=7.5e-3)
