@@ -125,3 +125,25 @@ def test_training_step_tolerance_leaves_room_beyond_bf16_storage(S, P, hidden, H
     dx, dw = O.qkv_projection_backward(x, w, g.reshape(S, -1))
     for name, got, ref in (("dqkv", g, rdqkv), ("dx", _bf16(dx), rdx), ("dw", dw, rdw)):
         assert_rel(got, ref, name, rel_max=1e-2, rel_norm=7.5e-3)
+
+
+@pytest.mark.parametrize("S,P,hidden,H,G,D,theta", [(1024, 4, 512, 8, 8, 64, 0.0),
+                                                    (2048, 8, 4096, 32, 8, 128, 500000.0)])
+def test_layer_tolerance_leaves_room_beyond_bf16_storage(S, P, hidden, H, G, D, theta):
+    """The whole-layer test holds y, dWo (and dx, dW, covered above) to the same tolerance.
+    Storing the attention output, y and dO as bf16, with everything else exact, must use at
+    most half of it."""
+    x = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_X, (S, hidden)))
+    w = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_W, ((H + 2 * G) * D, hidden),
+                                                    std=0.02))
+    wo = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_WO, (hidden, H * D), std=0.02))
+    dy = synthetic.bf16_to_f64(synthetic.normal_bf16(synthetic.SEED_DO, synthetic.TENSOR_WO, (S, hidden)))
+    o_seq, _, _ = O.ulysses_block_forward(x, w, P, H, G, D, theta)
+    o = o_seq.reshape(S, H, D)
+    ry = O.output_projection(o, wo)
+    rdo, rdwo = O.output_projection_backward(o, wo, dy)
+    o16 = _bf16(o)
+    y = _bf16(O.output_projection(o16, wo))
+    do, dwo = O.output_projection_backward(o16, wo, dy)
+    for name, got, ref in (("y", y, ry), ("dO", _bf16(do), rdo), ("dWo", dwo, rdwo)):
+        assert_rel(got, ref, name, rel_max=1e-2, rel_norm=7.5e-3)
