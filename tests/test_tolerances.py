@@ -147,3 +147,61 @@ def test_layer_tolerance_leaves_room_beyond_bf16_storage(S, P, hidden, H, G, D, 
     do, dwo = O.output_projection_backward(o16, wo, dy)
     for name, got, ref in (("y", y, ry), ("dO", _bf16(do), rdo), ("dWo", dwo, rdwo)):
         assert_rel(got, ref, name, rel_max=1e-2, rel_norm=7.5e-3)
+
+
+# ------------------------------------------------------------------------------ RoPE
+ROPE_L = 1024   # the split of a position into s = sh * ROPE_L + sl used by the table
+
+
+def _rope_fp32(x, pos, theta, D):
+    """The permute kernel's RoPE: (cos, sin)(s w_i) rebuilt in fp32 by angle addition from a
+    two-level table of fp32 values computed in fp64 (hi: sh * ROPE_L * w_i, lo: sl * w_i),
+    then the pair rotation in fp32 (numpy rounds each product, so this is slightly coarser
+    than the kernel's fused multiply-adds) and one bf16 rounding."""
+    f32 = np.float32
+    w = theta ** (-2.0 * np.arange(D // 2) / D)
+    sh, sl = pos // ROPE_L, pos % ROPE_L
+    a, b = np.outer(sh * ROPE_L, w), np.outer(sl, w)
+    a_c, a_s = np.cos(a).astype(f32), np.sin(a).astype(f32)
+    b_c, b_s = np.cos(b).astype(f32), np.sin(b).astype(f32)
+    cs = a_c * b_c - a_s * b_s
+    sn = a_s * b_c + a_c * b_s
+    lo, hi = x[..., :D // 2].astype(f32), x[..., D // 2:].astype(f32)
+    cs, sn = cs[:, None, :], sn[:, None, :]
+    return _bf16(np.concatenate([lo * cs - hi * sn, hi * cs + lo * sn], axis=-1)), (cs, sn, w)
+
+
+def _rope_positions():
+    rng = np.random.default_rng(5)
+    far = rng.integers(0, 1 << 20, 2048)
+    return np.unique(np.concatenate([np.arange(64), far, [(1 << 20) - 1]]))
+
+
+def test_rope_bound_admits_the_two_level_table():
+    """The GPU test holds RoPE to one bf16 ulp (at the exact value) + 1e-5 against the fp64
+    rotation of the same bf16 input, at positions up to 2^20."""
+    D, theta = 128, 500000.0
+    pos = _rope_positions()
+    x = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_QKV, (pos.size, 4, D), std=1.28))
+    got, (cs, sn, w) = _rope_fp32(x, pos, theta, D)
+    ang = np.outer(pos, w)
+    assert np.abs(cs[:, 0] - np.cos(ang)).max() < 1e-6 and np.abs(sn[:, 0] - np.sin(ang)).max() < 1e-6
+    ref = O.apply_rope(x, pos, theta)
+    err = np.abs(got - ref)
+    assert np.all(err <= bf16_ulp(ref) + 1e-5), (err / (bf16_ulp(ref) + 1e-5)).max()
+
+
+def test_rope_bound_catches_an_fp32_angle():
+    """Forming the angle s * w_i itself in fp32 (instead of the fp64 table) loses it at
+    large positions: the bound catches that."""
+    D, theta = 128, 500000.0
+    pos = _rope_positions()
+    x = synthetic.bf16_to_f64(synthetic.normal_bf16(0, synthetic.TENSOR_QKV, (pos.size, 4, D), std=1.28))
+    f32 = np.float32
+    w = (theta ** (-2.0 * np.arange(D // 2) / D)).astype(f32)
+    ang = pos.astype(f32)[:, None] * w[None, :]
+    cs, sn = np.cos(ang).astype(f32)[:, None, :], np.sin(ang).astype(f32)[:, None, :]
+    lo, hi = x[..., :D // 2].astype(f32), x[..., D // 2:].astype(f32)
+    got = _bf16(np.concatenate([lo * cs - hi * sn, hi * cs + lo * sn], axis=-1))
+    ref = O.apply_rope(x, pos, theta)
+    assert np.any(np.abs(got - ref) > bf16_ulp(ref) + 1e-5)
