@@ -205,3 +205,22 @@ def test_rope_bound_catches_an_fp32_angle():
     got = _bf16(np.concatenate([lo * cs - hi * sn, hi * cs + lo * sn], axis=-1))
     ref = O.apply_rope(x, pos, theta)
     assert np.any(np.abs(got - ref) > bf16_ulp(ref) + 1e-5)
+
+
+# ------------------------------------------------------------- the fixed target bound
+def test_fixed_bound_leaves_margin_at_the_8b_head_shape():
+    """Outside the peaked case the GPU tests hold attention to max|err| <= max(2e-2, one bf16
+    ulp) and mean|err| <= 2e-3 (the target's bound).  At the 8B head shape (S=2048, P=8,
+    rank 0: 4 query heads on one KV head, q/k/v std 1.28) the kernels' roundings use about
+    half of the max bound and a tenth of the mean bound."""
+    S, P, H, G, D, std = 2048, 8, 32, 8, 128, 1.28
+    f = lambda bits: synthetic.bf16_to_f64(bits)[0]
+    q = f(synthetic.normal_bf16(0, synthetic.TENSOR_Q, (P, S, H // P, D), std=std))
+    k = f(synthetic.normal_bf16(0, synthetic.TENSOR_K, (P, S, G // P, D), std=std))
+    v = f(synthetic.normal_bf16(0, synthetic.TENSOR_V, (P, S, G // P, D), std=std))
+    do = f(synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D)))
+    o, _ = O.causal_attention(q, k, v)
+    ref = (o,) + O.causal_attention_bwd(q, k, v, do)
+    for name, got, r in zip(("o", "dq", "dk", "dv"), _simulate(q, k, v, do, _f16, _f16), ref):
+        e = np.abs(got - r)
+        assert (e / np.maximum(2e-2, bf16_ulp(r))).max() <= 0.6 and e.mean() <= 0.25 * 2e-3, name
