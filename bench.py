@@ -66,9 +66,13 @@ def load_peaks():
     try:
         with open(path) as f:
             d = json.load(f)
-        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+        peaks = {k: float(d[k]) for k in FALLBACK_PEAKS}
+        # the median SM clock under load while the sustained GEMM peak was measured
+        clk = (d.get("clocks_under_load") or {}).get("sm_mhz_median")
+        peaks["sustained_sm_mhz"] = float(clk) if clk else None
+        return peaks, "measured"
     except Exception:
-        return dict(FALLBACK_PEAKS), "fallback"
+        return dict(FALLBACK_PEAKS, sustained_sm_mhz=None), "fallback"
 
 
 def reduce_max_ms(ms, world, dist=None, device=None):
@@ -244,9 +248,9 @@ def run_ours(args):
     sid = stream.cuda_stream
     names = ["qkv_proj", "seq_to_head", "attn_fwd", "head_to_seq_o", "seq_to_head_do",
              "attn_bwd", "head_to_seq_grads"]
-    # qkv_proj, seq_to_head, attn_fwd, head_to_seq (O), seq_to_head (dO), attn_bwd (pre, two
-    # fp16 copies, main, dQ conversion), head_to_seq of the gradients
-    launches_per_step = 1 + 1 + 1 + 1 + 1 + 5 + 1
+    # qkv_proj, seq_to_head, attn_fwd, head_to_seq (O), seq_to_head (dO), attn_bwd (largest
+    # magnitudes, pre, two fp16 copies, main, dQ conversion), head_to_seq of the gradients
+    launches_per_step = 1 + 1 + 1 + 1 + 1 + 6 + 1
 
     def step(ev=None, io=None, sync=None):
         # io: the step's input and output buffers (x, dO_seq, o_seq, dqkv_seq)
@@ -464,7 +468,7 @@ def run_ours(args):
                  "o_proj_tflops": oproj_f / (lper["o_proj"] * 1e-3) / 1e12,
                  "o_proj_bwd_tflops": 2 * oproj_f / (lper["o_proj_bwd"] * 1e-3) / 1e12,
                  "qkv_proj_bwd_tflops": 2 * proj_f / (lper["qkv_proj_bwd"] * 1e-3) / 1e12,
-                 "launches_per_step": 1 + 1 + 1 + 1 + 2 + 5 + 1 + 2}
+                 "launches_per_step": 1 + 1 + 1 + 1 + 2 + 6 + 1 + 2}
 
     # Ring attention (what "Snowflake's Ulysses trick ..." para 3 compares Ulysses with) on
     # the same virtual ranks and tokens: its forward with the K/V exchange, beside the
@@ -509,6 +513,19 @@ def run_ours(args):
         cpu = {"value": f / s / 1e12, "unit": "TFLOPS", "cores": host_cores(), "kind": "oracle",
                "sample": desc, "seconds": s}
 
+    clocks = clk.summary()
+
+    def fractions(tflops):
+        # against the sustained peak (for a kernel inside a long step), the burst peak, and
+        # the sustained peak with the kernel's time taken at the clock the peak was measured
+        # at (time x bench SM MHz / peak SM MHz), so that a faster clock here flatters nothing
+        f = {"frac_sustained": tflops / peaks["bf16_tflops_sustained"],
+             "frac_burst": tflops / peaks["bf16_tflops"]}
+        if clocks.get("sm_mhz") and peaks.get("sustained_sm_mhz"):
+            f["frac_sustained_at_peak_clock"] = (tflops * peaks["sustained_sm_mhz"] / clocks["sm_mhz"]
+                                                 / peaks["bf16_tflops_sustained"])
+        return f
+
     if rank == 0:
         peak = peaks["bf16_tflops_sustained"]
         line = {
@@ -520,17 +537,22 @@ def run_ours(args):
                        "n_q_heads": H, "n_kv_heads": G, "head_dim": D, "rope_theta": theta,
                        "global_batch": world, "parallelism": "replicas" if world > 1 else "single",
                        "l2": "inputs larger than L2 (no flush)"},
-            "roofline": {"kernel": "ulysses_attn_bwd", "bound": "tensor",
-                         "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
-                         "frac": bwd_tflops / peak, "traffic": bwd_traffic(S),
-                         "peak_source": "%s bf16_tflops_sustained" % peak_kind},
+            "roofline": dict({"kernel": "ulysses_attn_bwd", "bound": "tensor",
+                              "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                              "frac": bwd_tflops / peak, "traffic": bwd_traffic(S),
+                              "peak_source": "%s bf16_tflops_sustained" % peak_kind,
+                              "peak_burst": peaks["bf16_tflops"],
+                              "sm_mhz": clocks.get("sm_mhz"),
+                              "peak_sustained_sm_mhz": peaks.get("sustained_sm_mhz")},
+                             **fractions(bwd_tflops)),
             "kernels_ms": avg,
             "attn_fwd_tflops": fwd_tflops, "attn_bwd_tflops": bwd_tflops,
-            "attn_fwd_frac": fwd_tflops / peak, "qkv_proj_tflops": qkv_tflops,
+            "attn_fwd_frac": fwd_tflops / peak, "attn_fwd_fractions": fractions(fwd_tflops),
+            "qkv_proj_tflops": qkv_tflops,
             "permute_gbs": perm_gbs, "permute_frac_hbm": perm_gbs / peaks["hbm_gbs"],
             "seq_to_head_gbs": s2h_gbs, "peaks": peaks, "peaks_source": peak_kind,
             "gpu_launches": launches_per_step * args.steps,
-            "clocks": clk.summary(), "e2e": e2e, "cpu_baseline": cpu,
+            "clocks": clocks, "e2e": e2e, "cpu_baseline": cpu,
             "layer_train_step": layer, "ring_attention": ring,
         }
         print(json.dumps(line))

@@ -39,8 +39,12 @@
  *     stream) and return a uly_status at once.  They never throw or exit.
  *   - On error nothing is launched and ulysses_last_error() describes the problem (a
  *     thread-local string valid until the next call on the same thread).
- *   - Device-side failures (a wait that ran out, an unexpected layout) are recorded in a
- *     status word held by the plan; ulysses_sync_status() reads and clears it.
+ *   - Device-side failures (a wait that ran out, an input out of range) are recorded in a
+ *     status word held by the plan; ulysses_sync_status() reads and clears it.  The word
+ *     is sticky: while it holds an error, every kernel of every later call on the same plan
+ *     gives up at its first wait that does not complete at once, so those calls' outputs
+ *     are undefined.  After a failure, call ulysses_sync_status() (which clears the word)
+ *     before relying on the plan again.
  *   - S = 0 is valid: every call is a no-op that returns ULY_OK.
  */
 #ifndef ULYSSES_H_
@@ -59,7 +63,9 @@ typedef enum uly_status {
   ULY_ERR_UNSUPPORTED = 2,  /* valid in principle, not built here (e.g. D not 64/128) */
   ULY_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
   ULY_ERR_OOM = 4,          /* the plan could not allocate its own small buffers */
-  ULY_ERR_TIMEOUT = 5       /* a device-side wait ran past its limit (from sync_status) */
+  ULY_ERR_TIMEOUT = 5,      /* a device-side wait ran past its limit (from sync_status) */
+  ULY_ERR_RANGE = 6         /* an input's magnitude lies beyond what the backward's scaled
+                               fp16 operands can hold (from sync_status) */
 } uly_status;
 
 /* Plan flags. */
@@ -137,6 +143,14 @@ uly_status ulysses_attn_fwd(uly_plan plan, const void *q, const void *k, const v
  * NULL: the row terms then use the bf16 o alone) and the upstream gradient d_o in head
  * layout [P][S][H/P][D].  Outputs dq [P][S][H/P][D], dk, dv [P][S][G/P][D] in bf16; dk
  * and dv sum the contributions of all query heads of a KV head.
+ * The tensor-core operands are fp16 copies of q, k, v and d_o, each multiplied by a power
+ * of two chosen per call from the tensor's largest magnitude (and the products P, dS kept
+ * in fp16 range), with the inverse powers applied exactly to the outputs.  So gradients as
+ * small as a training step's (|d_o| ~ 1e-8) keep fp16's full precision, bf16 inputs above
+ * fp16's 65504 are not clipped, and scaling any input by a power of two scales the outputs
+ * by exactly that factor.  Only a tensor whose largest magnitude is below 2^-53 or above
+ * 2^67 (q, k, v) -- beyond the exponents' range -- cannot be fully normalised; if an fp16
+ * copy would then saturate, the call reports ULY_ERR_RANGE through the status word.
  * workspace: ulysses_workspace_bytes(plan) bytes of device memory (fp32 accumulators);
  * its contents on entry do not matter. */
 uly_status ulysses_attn_bwd(uly_plan plan, const void *q, const void *k, const void *v,
@@ -149,12 +163,13 @@ uly_status ulysses_attn_bwd(uly_plan plan, const void *q, const void *k, const v
  * has handed all of HBM to its own pool or caching allocator, a latency-critical path
  * that must not pay cudaMalloc's implicit synchronisation, a plain C caller without a
  * device allocator.  Same arguments and results as ulysses_attn_bwd (minus workspace).
- * The scratch is a fixed 64 MiB array inside the library's device memory (held by every
- * GPU that loads the library until the process exits); plans whose backward needs more
- * (ulysses_workspace_bytes) get ULY_ERR_UNSUPPORTED and nothing is launched.  The first
- * call on each device looks the array's address up (make it before any stream capture);
- * no call allocates.  All calls share the array: calls that may overlap on the GPU race,
- * so order them (e.g. one stream).  The plan's device must be the current device. */
+ * The scratch is a fixed 64 MiB array inside the library's device memory.  A GPU holds it
+ * from the first ulysses_plan made on it (with eager module loading: from the library's
+ * load) until the process exits; ulysses_plan looks its address up, so no call of this
+ * entry point, its first included, allocates or loads anything.  Plans whose backward
+ * needs more scratch (ulysses_workspace_bytes) get ULY_ERR_UNSUPPORTED and nothing is
+ * launched.  All calls share the array: calls that may overlap on the GPU race, so order
+ * them (e.g. one stream).  The plan's device must be the current device. */
 uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void *q, const void *k,
                                     const void *v, const void *o, const void *o_lo,
                                     const float *lse, const void *d_o, void *dq, void *dk,
@@ -206,7 +221,9 @@ uly_status ulysses_o_proj_bwd(uly_plan plan, const void *o_head, const void *wo,
                               const void *dy, void *do_head, float *dwo, void *stream);
 
 /* Synchronises `stream`, reads the plan's device status word, clears it and returns it
- * (ULY_OK, or e.g. ULY_ERR_TIMEOUT).  ULY_ERR_CUDA if the synchronisation itself fails. */
+ * (ULY_OK, or e.g. ULY_ERR_TIMEOUT, ULY_ERR_RANGE).  ULY_ERR_CUDA if the synchronisation
+ * itself fails.  Until it is called after a device-side failure, the plan's later calls
+ * abort early (see the conventions above). */
 uly_status ulysses_sync_status(uly_plan plan, void *stream);
 
 /* Bytes read plus written by this plan's permute kernels since it was made: what the

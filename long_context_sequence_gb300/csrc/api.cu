@@ -238,6 +238,10 @@ uly_status ulysses_plan(const uly_config* cfg, uly_plan* out) {
       return s;
     }
   }
+  // The allocation-free backward's scratch address, looked up here so that no call of
+  // ulysses_attn_bwd_noalloc ever loads device code or allocates.  A failure only disables
+  // that entry point (it reports the error); the rest of the plan works without it.
+  uly::noalloc_setup(p);
   *out = h;
   uly::g_err[0] = 0;
   return ULY_OK;
@@ -407,6 +411,9 @@ uly_status ulysses_sync_status(uly_plan plan, void* stream) {
     if (st == ULY_ERR_TIMEOUT)
       return fail(ULY_ERR_TIMEOUT, "a device-side wait ran past %llu ms",
                   (unsigned long long)(plan->p.limit_ns / 1000000ull));
+    if (st == ULY_ERR_RANGE)
+      return fail(ULY_ERR_RANGE, "an attention-backward input's largest magnitude is beyond "
+                                 "the range its scaled fp16 copy can hold");
     return fail((uly_status)st, "device reported status %d", st);
   }
   uly::g_err[0] = 0;

@@ -26,13 +26,26 @@
 //               the same warps, thread = d: dQ^T -> fp32 reductions into the workspace
 //                      accumulator (one 128-byte run per warp and row);
 //   bwd_dq    fp32 dQ accumulator -> bf16.
-// Every MMA runs on fp16 operands: the fp16 copies of Q, K, V, dO made by the pre-pass
-// (exact for magnitudes in [2^-14, 65504]; saturated outside), and P, dS keep 11
-// significand bits, which the long dK/dQ sums need.  P is formed as scale * P (the scale
-// folded into the exponent), so dS, dQ^T and dK come out scaled and dV is divided by the
-// scale once at the end.
+// Every MMA runs on fp16 operands, and P, dS keep 11 significand bits, which the long
+// dK/dQ sums need.  fp16 holds full precision only in [2^-14, 65504], while the bf16 inputs
+// span fp32's range (a training step's dO is often 1e-5 .. 1e-8, and q, k, v may exceed
+// 65504).  So every operand is scaled by an exact power of two chosen per call from the
+// tensors' largest magnitudes (bwd_amax_kernel):
+//   q' = 2^eq q, k' = 2^ek k      largest |x'| in [2^7, 2^8)
+//   v' = 2^ev v                   largest |v'| in [2^-1, 2^0)
+//   P' = 2^kp scale P             2^kp scale in [2^7, 2^8)  (kp fixed by the plan's scale)
+//   dO' = 2^edo dO                the largest edo with 2^kp scale D max|dO'| max|v'| <= 2^14
+//                                 and max|dO'| < 2^15
+// Then |dP' - D'| <= 2 D max|dO'| max|v'| and dS' = P' (dP' - D') stays below 2^15: no fp16
+// operand can overflow, and for ordinary data none is subnormal.  The outputs take the
+// inverse powers exactly (ldexp in the epilogues): dV = acc / (scale 2^(kp+edo)),
+// dK = 2^-(kp+edo+ev+eq) acc, dQ = 2^-(kp+edo+ev+ek) acc.  Scaling any input by a power of
+// two therefore leaves every fp16 operand bit for bit as it was and scales the outputs
+// exactly.  A tensor whose largest magnitude lies beyond the exponents' range (|e| <= 60)
+// would saturate: the call reports ULY_ERR_RANGE through the status word.
 // TMEM (512 columns): region X at [128X, 128X+128): S^T [0,64) -> dQ^T; dP^T [64,128) ->
 // P^T of warpgroup w2 at [64+32 w2, 64+32 w2+16).  dV [256,256+D), dK [256+D, 256+2D).
+#include <cmath>
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -68,11 +81,13 @@ struct BwdLayout {
 struct BwdArgs {
   const float* lse;
   const float* delta;
+  const int* exps;        // the call's exponents eq, ek, ev, edo (bwd_amax_kernel)
   float* dq_acc;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
   int S, hl, gl, group, nkb;
-  float scale, scale_log2, log2_scale;
+  int kp;                 // P' = 2^kp scale P
+  float scale, scale_log2, log2_scale;   // log2_scale = log2(scale) + kp
   int* status;
   uint64_t limit_ns;
   uint32_t flags;
@@ -137,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 13);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
+  float* sl2_s = reinterpret_cast<float*>(abort_flag + 5);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int per_rank = a.gl * a.nkb;
@@ -163,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(drain_acc, 1);
     *abort_flag = 0;
+    // s' = q'.k' = 2^(eq+ek) q.k: the exponent's multiplier takes the inverse power
+    *sl2_s = a.scale_log2 * exp2i(-(a.exps[0] + a.exps[1]));
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -339,7 +357,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int key_g = nb * BN + row;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t treg = tbase + lane_off + 128 * X;
-    const float sl2 = a.scale_log2;
     uint8_t* ds_row = smem + L::kDS + X * kBox + row * 128;
     // The region's first warp waits on the mbarrier; the other seven sleep in a named
     // barrier (no issue slots) and read the outcome it left, so they all decide alike.
@@ -396,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             nl[i2] = f2_pack(n0, n1);
           }
         }
+        const float sl2 = *sl2_s;
         const uint64_t sc2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {
@@ -466,7 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int which = warp / 8;         // 0: dV, 1: dK
       const int half = w2;                // columns [half * D/2, (half + 1) * D/2)
       __nv_bfloat16* dst = (which ? a.dk : a.dv) + (((size_t)r * a.S + key_g) * a.gl + gg) * D;
-      const float mul = which ? 1.f : 1.f / a.scale;   // the dV sums carry the scale
+      // dV sums carry 2^(kp+edo) scale, dK sums 2^(kp+edo+ev+eq)
+      const int4 ex = __ldcg(reinterpret_cast<const int4*>(a.exps));   // read here, not earlier
+      const float mul = which ? 1.f : 1.f / a.scale;
+      const int sh = which ? -(a.kp + ex.w + ex.z + ex.x) : -(a.kp + ex.w);
+      // 2^sh as two factors of the same sign (|sh| may exceed a float exponent's range)
+      const float m1 = mul * exp2i(sh / 2), m2 = exp2i(sh - sh / 2);
 #pragma unroll 1
       for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t v[32];
@@ -474,11 +497,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (key_g < a.S) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
+            auto sc = [&](int e) { return __uint_as_float(v[8 * j + e]) * m1 * m2; };
             uint4 o;
-            o.x = pack_bf16x2(__uint_as_float(v[8 * j + 0]) * mul, __uint_as_float(v[8 * j + 1]) * mul);
-            o.y = pack_bf16x2(__uint_as_float(v[8 * j + 2]) * mul, __uint_as_float(v[8 * j + 3]) * mul);
-            o.z = pack_bf16x2(__uint_as_float(v[8 * j + 4]) * mul, __uint_as_float(v[8 * j + 5]) * mul);
-            o.w = pack_bf16x2(__uint_as_float(v[8 * j + 6]) * mul, __uint_as_float(v[8 * j + 7]) * mul);
+            o.x = pack_bf16x2(sc(0), sc(1));
+            o.y = pack_bf16x2(sc(2), sc(3));
+            o.z = pack_bf16x2(sc(4), sc(5));
+            o.w = pack_bf16x2(sc(6), sc(7));
             *reinterpret_cast<uint4*>(dst + 32 * c + 8 * j) = o;
           }
         }
@@ -496,8 +520,116 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// D_i = sum_d dO_i[d] * (O_i[d] + O_lo_i[d]) (fp32) and zeroing of the dQ accumulator
-// rows.  16 threads per row of D = 128 (8 elements each), 8 per row of D = 64.
+// Largest magnitudes of q, k, v and dO for the call's power-of-two scaling, then (in the
+// last block to finish) the exponents.
+// The rule, with E(m) = floor(log2 m) and every exponent clamped to [-60, 60] (so every
+// sum of two of them, and of kp, is a float exponent):
+//   eq = 7 - E(max|q|), ek = 7 - E(max|k|)     -> max|q'|, max|k'| in [2^7, 2^8)
+//   ev = -1 - E(max|v|)                        -> max|v'| in [2^-1, 2^0)
+//   edo = min(14 - E(max|dO|), 13 - E(X)), X = 2^kp scale D max|dO| max|v'|
+//                                              -> max|dO'| < 2^15 and X 2^edo < 2^14
+// A zero (or non-finite) maximum leaves its exponent at 0.  A tensor whose scaled maximum
+// would still reach 2^15 (only possible when the clamp bites) makes the call report
+// kErrRange: its fp16 copy would saturate.
+__device__ __forceinline__ bool finite_pos(float m) { return m > 0.f && m <= 3.4028234e38f; }
+__device__ __forceinline__ int clamp_exp(int e) { return e < -60 ? -60 : (e > 60 ? 60 : e); }
+// floor(log2 m) of a positive finite float, subnormals included.
+__device__ __forceinline__ int floor_log2f(float m) {
+  const uint32_t b = __float_as_uint(m);
+  const int ex = (int)((b >> 23) & 0xFFu);
+  return ex ? ex - 127 : (31 - __clz((int)(b & 0x7FFFFFu))) - 149;
+}
+
+__device__ void bwd_exponents(const float (&M)[4], float scale_k, int D, int (&e)[4],
+                              bool& range) {
+  e[0] = finite_pos(M[0]) ? clamp_exp(7 - floor_log2f(M[0])) : 0;
+  e[1] = finite_pos(M[1]) ? clamp_exp(7 - floor_log2f(M[1])) : 0;
+  e[2] = finite_pos(M[2]) ? clamp_exp(-1 - floor_log2f(M[2])) : 0;
+  int edo = 0;
+  if (finite_pos(M[3])) {
+    edo = 14 - floor_log2f(M[3]);
+    const float sd = scale_k * (float)D;
+    if (finite_pos(M[2]) && finite_pos(sd)) {
+      // X as a product of mantissas in [1, 2) times a power of two (nothing overflows)
+      const int a = floor_log2f(sd), b = floor_log2f(M[3]), c = floor_log2f(M[2]);
+      const float mm = ldexpf(sd, -a) * ldexpf(M[3], -b) * ldexpf(M[2], -c);
+      const int ex = a + b + c + e[2] + floor_log2f(mm);
+      edo = min(edo, 13 - ex);
+    }
+    edo = clamp_exp(edo);
+  }
+  e[3] = edo;
+  range = false;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (finite_pos(M[j]) && floor_log2f(M[j]) + e[j] >= 15) range = true;
+}
+
+// Largest |x| of 8 bf16 as the bit pattern of a non-negative bf16 (whose unsigned order is
+// the order of the magnitudes).
+__device__ __forceinline__ uint32_t absmax8_bits(uint4 v) {
+  const uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                              __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+  return max(m & 0xFFFFu, m >> 16);
+}
+
+// scal (zeroed before the launch): [0, 4) largest |q|, |k|, |v|, |dO| as fp32 bit patterns,
+// [4] count of finished blocks, [8, 12) the exponents eq, ek, ev, edo.
+__global__ void __launch_bounds__(256) bwd_amax_kernel(const uint4* __restrict__ q,
+                                                       const uint4* __restrict__ k,
+                                                       const uint4* __restrict__ v,
+                                                       const uint4* __restrict__ d_o,
+                                                       int64_t nq8, int64_t nk8,
+                                                       uint32_t* scal, float scale_k, int D,
+                                                       int* status) {
+  uint32_t m[4] = {0u, 0u, 0u, 0u};
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t t0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t i = t0; i < nq8; i += stride) {
+    m[0] = max(m[0], absmax8_bits(__ldcs(q + i)));
+    m[3] = max(m[3], absmax8_bits(__ldcs(d_o + i)));
+  }
+  for (int64_t i = t0; i < nk8; i += stride) {
+    m[1] = max(m[1], absmax8_bits(__ldcs(k + i)));
+    m[2] = max(m[2], absmax8_bits(__ldcs(v + i)));
+  }
+  __shared__ uint32_t red[8][4];
+  __shared__ bool last;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m[j] = max(m[j], __shfl_xor_sync(0xffffffffu, m[j], off));
+  }
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (lane == 0)
+    for (int j = 0; j < 4; ++j) red[warp][j] = m[j];
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < 4; ++j) {
+      uint32_t x = 0;
+      for (int w = 0; w < (int)(blockDim.x / 32); ++w) x = max(x, red[w][j]);
+      atomicMax(&scal[j], x << 16);     // bf16 bits -> fp32 bits
+    }
+    __threadfence();
+    last = atomicAdd(&scal[4], 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (last && threadIdx.x == 0) {
+    __threadfence();
+    float M[4];
+    for (int j = 0; j < 4; ++j) M[j] = __uint_as_float(atomicOr(&scal[j], 0u));
+    int e[4];
+    bool range;
+    bwd_exponents(M, scale_k, D, e, range);
+    int* ex = reinterpret_cast<int*>(scal + 8);
+    for (int j = 0; j < 4; ++j) ex[j] = e[j];
+    if (range) atomicCAS(status, kOk, kErrRange);
+  }
+}
+
+// D'_i = 2^(edo+ev) sum_d dO_i[d] * (O_i[d] + O_lo_i[d]) (fp32), zeroing of the dQ
+// accumulator rows and the fp16 copies q' = 2^eq q and dO' = 2^edo dO.  16 threads per row
+// of D = 128 (8 elements each), 8 per row of D = 64.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ o_lo,
@@ -507,8 +639,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ dq_acc,
                                                       uint4* __restrict__ q16,
                                                       uint4* __restrict__ do16, int64_t rows,
-                                                      int64_t S, int hl) {
+                                                      int64_t S, int hl,
+                                                      const int* __restrict__ exps) {
   constexpr int TPR = D / 8;
+  const int4 ex = *reinterpret_cast<const int4*>(exps);
   const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t rowid = tid / TPR;       // row in [P][S][hl] order
   const int part = (int)(tid % TPR);
@@ -531,10 +665,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     float4* zq = reinterpret_cast<float4*>(dq_acc + rowid * D + part * 8);
     zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
-    // fp16 copies of dO and Q for the main kernel's tensor-core operands
-    do16[(rowid * D + part * 8) / 8] = bf16x8_to_f16x8(b);
-    q16[(rowid * D + part * 8) / 8] =
-        bf16x8_to_f16x8(*reinterpret_cast<const uint4*>(q + rowid * D + part * 8));
+    // fp16 copies of dO' and q' for the main kernel's tensor-core operands
+    do16[(rowid * D + part * 8) / 8] = bf16x8_to_f16x8_scaled(b, exp2i(ex.w));
+    q16[(rowid * D + part * 8) / 8] = bf16x8_to_f16x8_scaled(
+        *reinterpret_cast<const uint4*>(q + rowid * D + part * 8), exp2i(ex.x));
   }
 #pragma unroll
   for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -542,31 +676,47 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const int64_t hh = rowid % hl;
     const int64_t rs = rowid / hl;     // r * S + s
     const int64_t r = rs / S, s = rs - r * S;
-    delta[(r * hl + hh) * S + s] = acc;
+    delta[(r * hl + hh) * S + s] = acc * exp2i(ex.w + ex.z);
   }
 }
 
-// bf16 -> fp16 copy, 8 elements per thread (K and V for the main kernel).
+// bf16 -> fp16 copy scaled by 2^exps[which], 8 elements per thread (k' and v' for the main
+// kernel).
 __global__ void __launch_bounds__(256) to_f16_kernel(const uint4* __restrict__ src,
-                                                     uint4* __restrict__ dst, int64_t n8) {
+                                                     uint4* __restrict__ dst, int64_t n8,
+                                                     const int* __restrict__ exps, int which) {
+  const float p2 = exp2i(exps[which]);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = bf16x8_to_f16x8(src[i]);
+    dst[i] = bf16x8_to_f16x8_scaled(src[i], p2);
 }
 
+// fp32 dQ accumulator (which holds 2^(kp+edo+ev+ek) dQ) -> bf16 dQ.
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
-                                                     __nv_bfloat16* __restrict__ dq, int64_t n8) {
+                                                     __nv_bfloat16* __restrict__ dq, int64_t n8,
+                                                     const int* __restrict__ exps, int kp) {
+  const int4 ex = *reinterpret_cast<const int4*>(exps);
+  const int sh = -(kp + ex.w + ex.z + ex.y);
+  const float m1 = exp2i(sh / 2), m2 = exp2i(sh - sh / 2);   // 2^sh, same-sign factors
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
     const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
     uint4 v;
-    v.x = pack_bf16x2(a.x, a.y);
-    v.y = pack_bf16x2(a.z, a.w);
-    v.z = pack_bf16x2(b.x, b.y);
-    v.w = pack_bf16x2(b.z, b.w);
+    v.x = pack_bf16x2(a.x * m1 * m2, a.y * m1 * m2);
+    v.y = pack_bf16x2(a.z * m1 * m2, a.w * m1 * m2);
+    v.z = pack_bf16x2(b.x * m1 * m2, b.y * m1 * m2);
+    v.w = pack_bf16x2(b.z * m1 * m2, b.w * m1 * m2);
     reinterpret_cast<uint4*>(dq)[i] = v;
   }
+}
+
+// kp of the plan's scale: 2^kp scale in [2^7, 2^8) (kp within [-30, 30]).
+int p_exponent(float scale) {
+  int e = 0;
+  std::frexp(scale, &e);            // scale = f 2^e, f in [0.5, 1)
+  int kp = 8 - e;
+  return kp < -30 ? -30 : (kp > 30 ? 30 : kp);
 }
 
 template <int D>
@@ -582,23 +732,34 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   void* do16 = wsb + ws.do16;
   void* k16 = wsb + ws.k16;
   void* v16 = wsb + ws.v16;
+  uint32_t* scal = reinterpret_cast<uint32_t*>(wsb + ws.scal);
+  const int* exps = reinterpret_cast<const int*>(scal + 8);
+  const int kp = p_exponent(p.scale);
   const int64_t rows = (int64_t)p.P * p.S * hl;
+  const int64_t cap = (int64_t)num_sms(p.device) * 16;
   {
+    cudaError_t e = cudaMemsetAsync(scal, 0, 64, st);
+    if (e != cudaSuccess) return e;
+    const int64_t nq8 = rows * D / 8, nk8 = (int64_t)p.P * p.S * gl * D / 8;
+    const int64_t ba = std::min<int64_t>((nq8 + 255) / 256, (int64_t)num_sms(p.device) * 8);
+    bwd_amax_kernel<<<(unsigned)std::max<int64_t>(ba, 1), 256, 0, st>>>(
+        static_cast<const uint4*>(q), static_cast<const uint4*>(k), static_cast<const uint4*>(v),
+        static_cast<const uint4*>(d_o), nq8, nk8, scal, std::ldexp(p.scale, kp), D, p.status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const int64_t threads = rows * (D / 8);
     const int64_t blocks = (threads + 255) / 256;
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(o_lo),
         static_cast<const __nv_bfloat16*>(d_o), static_cast<const __nv_bfloat16*>(q), delta,
-        dq_acc, static_cast<uint4*>(q16), static_cast<uint4*>(do16), rows, p.S, hl);
-    cudaError_t e = cudaGetLastError();
+        dq_acc, static_cast<uint4*>(q16), static_cast<uint4*>(do16), rows, p.S, hl, exps);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t n8 = (int64_t)p.P * p.S * gl * D / 8;
-    const int64_t cap = (int64_t)num_sms(p.device) * 16;
-    const int64_t b8 = std::min<int64_t>((n8 + 255) / 256, cap);
+    const int64_t b8 = std::min<int64_t>((nk8 + 255) / 256, cap);
     to_f16_kernel<<<(unsigned)b8, 256, 0, st>>>(static_cast<const uint4*>(k),
-                                                 static_cast<uint4*>(k16), n8);
+                                                 static_cast<uint4*>(k16), nk8, exps, 1);
     to_f16_kernel<<<(unsigned)b8, 256, 0, st>>>(static_cast<const uint4*>(v),
-                                                 static_cast<uint4*>(v16), n8);
+                                                 static_cast<uint4*>(v16), nk8, exps, 2);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -617,6 +778,8 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   BwdArgs a;
   a.lse = lse;
   a.delta = delta;
+  a.exps = exps;
+  a.kp = kp;
   a.dq_acc = dq_acc;
   a.dk = static_cast<__nv_bfloat16*>(dk);
   a.dv = static_cast<__nv_bfloat16*>(dv);
@@ -627,7 +790,7 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   a.nkb = (int)((p.S + BN - 1) / BN);
   a.scale = p.scale;
   a.scale_log2 = p.scale * 1.4426950408889634f;
-  a.log2_scale = log2f(p.scale);
+  a.log2_scale = log2f(p.scale) + (float)kp;
   a.status = p.status;
   a.limit_ns = p.limit_ns;
   a.flags = p.cfg.flags;
@@ -640,9 +803,9 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n8 = rows * D / 8;
-  const int64_t cap = (int64_t)num_sms(p.device) * 16;
   const int64_t blocks_dq = std::min<int64_t>((n8 + 255) / 256, cap);
-  bwd_dq_kernel<<<(unsigned)blocks_dq, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+  bwd_dq_kernel<<<(unsigned)blocks_dq, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
+                                                     exps, kp);
   return cudaGetLastError();
 }
 
@@ -659,6 +822,7 @@ BwdWorkspace bwd_workspace_layout(const Plan& p) {
   w.do16 = off;   off += al(P * S * hl * D * 2);
   w.k16 = off;    off += al(P * S * gl * D * 2);
   w.v16 = off;    off += al(P * S * gl * D * 2);
+  w.scal = off;   off += 256;
   w.total = off;
   return w;
 }

@@ -1,55 +1,58 @@
 // ulysses_attn_bwd_noalloc: the attention backward with its scratch held by the library.
 //
-// ulysses_attn_bwd needs a caller-provided workspace (an fp32 dQ accumulator and the fp32
-// row terms D_i).  Some callers cannot hand one over: a host program that has given all of
-// HBM to its own pool or caching allocator (a further cudaMalloc fails or fragments it), a
-// latency-critical path that must not pay cudaMalloc's implicit device synchronisation,
-// or a plain C caller that has no device allocator of its own.  For them this entry point
-// uses a fixed scratch array that lives in the library's own device memory.
+// ulysses_attn_bwd needs a caller-provided workspace (an fp32 dQ accumulator, the fp32 row
+// terms D_i and fp16 operand copies).  Some callers cannot hand one over: a host program
+// that has given all of HBM to its own pool or caching allocator (a further cudaMalloc
+// fails or fragments it), a latency-critical path that must not pay cudaMalloc's implicit
+// device synchronisation, or a plain C caller that has no device allocator of its own.
+// For them this entry point uses a fixed scratch array that lives in the library's own
+// device memory.
 //
-// The scratch is a file-scope __device__ array of kNoAllocScratchBytes (64 MiB): every GPU
-// that loads the library holds it until the process exits.  In host code the array's name
-// only stands for it; its device address is looked up once per device with
-// cudaGetSymbolAddress, on the first call made while that device is current.  Make that
-// first call before any stream capture.  The entry point itself never allocates (no
-// cudaMalloc, cudaFree or allocating library call).
+// The scratch is a file-scope __device__ array of kNoAllocScratchBytes (64 MiB).  A GPU
+// holds it from the moment this file's device code is loaded there until the process
+// exits: with the CUDA runtime's default lazy module loading that is the first
+// ulysses_plan on the device (which looks the array up, below), with eager loading the
+// load of the library.  In host code the array's name only stands for it; its device
+// address is looked up with cudaGetSymbolAddress in ulysses_plan, with the plan's device
+// current, and kept in the plan.  The entry point itself therefore never allocates (no
+// cudaMalloc, cudaFree, module load or allocating library call), its first call included.
+// A plan does not survive a reset of its device (cudaDeviceReset): make a new one.
 //
 // All calls share the one array and it keeps the last call's contents: the backward's
-// first kernel rewrites every byte it later reads (zeroes the dQ accumulator, writes D_i),
-// so nothing carries over from call to call.  Calls that overlap on the GPU (different
-// streams, no ordering between them) race on the array: order them.
+// first kernels rewrite every byte they later read (the largest-magnitude slots are
+// cleared, the dQ accumulator zeroed, D_i and the fp16 copies written), so nothing carries
+// over from call to call.  Calls that overlap on the GPU (different streams, no ordering
+// between them) race on the array: order them.
 #include <cstdio>
-#include <mutex>
 
 #include "uly_internal.h"
 
 namespace uly {
-namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(64) << 20;
-constexpr int kMaxDevices = 64;
 
+namespace {
 static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
 
-// Device address of g_bwd_scratch on `device` (which must be current).
-cudaError_t scratch_address(int device, void** out) {
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[device]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_bwd_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[device] = p;
+// Set-up, called by ulysses_plan with the plan's device current: the array's device
+// address on that device (loading this file's device code there if it is not yet loaded).
+cudaError_t noalloc_setup(Plan& p) {
+  void* addr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&addr, g_bwd_scratch);
+  if (e != cudaSuccess) {
+    cudaGetLastError();   // not sticky: leave no error behind for the caller's next call
+    p.noalloc_scratch = nullptr;
+    p.noalloc_setup_error = e;
+    return e;
   }
-  *out = g_scratch_addr[device];
+  p.noalloc_scratch = addr;
+  p.noalloc_setup_error = cudaSuccess;
   return cudaSuccess;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-}  // namespace
 }  // namespace uly
 
 extern "C" uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void* q, const void* k,
@@ -76,20 +79,20 @@ extern "C" uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void* q, con
     return set_error(ULY_ERR_UNSUPPORTED, msg);
   }
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return set_error(ULY_ERR_CUDA, "no current CUDA device");
+  if (cudaGetDevice(&dev) != cudaSuccess)
+    return set_error(ULY_ERR_CUDA, "cudaGetDevice failed (no usable CUDA device)");
   if (dev != p.device)
     return set_error(ULY_ERR_INVALID_ARG, "the plan's device is not the current device");
-  void* scratch = nullptr;
-  cudaError_t e = scratch_address(dev, &scratch);
-  if (e != cudaSuccess) {
+  if (!p.noalloc_scratch) {
     char msg[256];
-    snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the scratch array: %s",
-             cudaGetErrorString(e));
+    snprintf(msg, sizeof(msg),
+             "the scratch array's address could not be looked up when the plan was made "
+             "(cudaGetSymbolAddress: %s)",
+             cudaGetErrorString(p.noalloc_setup_error));
     return set_error(ULY_ERR_CUDA, msg);
   }
-  e = launch_attn_bwd(p, q, k, v, o, o_lo, lse, d_o, dq, dk, dv, scratch,
-                      reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_attn_bwd(p, q, k, v, o, o_lo, lse, d_o, dq, dk, dv, p.noalloc_scratch,
+                                  reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) {
     char msg[256];
     snprintf(msg, sizeof(msg), "attn_bwd_noalloc launch: %s", cudaGetErrorString(e));

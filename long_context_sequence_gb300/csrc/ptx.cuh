@@ -11,7 +11,7 @@ namespace uly {
 
 // Status codes shared with the C ABI (ulysses.h).
 enum : int { kOk = 0, kErrInvalid = 1, kErrUnsupported = 2, kErrCuda = 3, kErrOom = 4,
-             kErrTimeout = 5 };
+             kErrTimeout = 5, kErrRange = 6 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -341,6 +341,19 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
   return make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z),
                     bf16x2_to_f16x2(v.w));
+}
+// The same with every value multiplied by p2 (a power of two, so the product is exact and
+// the only rounding is the one to fp16).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_scaled(uint32_t w, float p2) {
+  return pack_f16x2_sat(__uint_as_float(w << 16) * p2, __uint_as_float(w & 0xFFFF0000u) * p2);
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_scaled(uint4 v, float p2) {
+  return make_uint4(bf16x2_to_f16x2_scaled(v.x, p2), bf16x2_to_f16x2_scaled(v.y, p2),
+                    bf16x2_to_f16x2_scaled(v.z, p2), bf16x2_to_f16x2_scaled(v.w, p2));
+}
+// 2^e as a float, for |e| <= 126.
+__device__ __forceinline__ float exp2i(int e) {
+  return __uint_as_float((uint32_t)(127 + e) << 23);
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

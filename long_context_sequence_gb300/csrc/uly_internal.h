@@ -27,7 +27,14 @@ struct Plan {
   int* status = nullptr;       // device status word
   uint64_t limit_ns = 0;
   std::atomic<uint64_t> bytes_moved{0};
+  // Device address of the library's fixed backward scratch on this plan's device (looked up
+  // when the plan is made), or null with the lookup's error.
+  void* noalloc_scratch = nullptr;
+  cudaError_t noalloc_setup_error = cudaSuccess;
 };
+
+// Looks up the fixed scratch array's device address for p (the plan's device current).
+cudaError_t noalloc_setup(Plan& p);
 
 // Records msg as the thread's last error (ULY_OK clears it) and returns s.
 uly_status set_error(uly_status s, const char* msg);
@@ -58,7 +65,8 @@ cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const v
                             cudaStream_t st);
 
 // Workspace layout of the backward pass (byte offsets, each 256-aligned): fp32 dQ
-// accumulator, fp32 row terms, fp16 copies of q, dO, k, v.
+// accumulator, fp32 row terms, fp16 copies of q, dO, k, v, and 256 bytes for the call's
+// largest magnitudes and power-of-two exponents.
 // Ring attention: K/V ring buffers (two sets, the steps alternate), the fp32 output
 // accumulator and the running max / sum of every row.
 struct RingWorkspace {
@@ -70,7 +78,7 @@ cudaError_t launch_ring_attn(const Plan& p, const void* q_seq, const void* k_seq
                              cudaStream_t st);
 
 struct BwdWorkspace {
-  size_t dq_acc, delta, q16, do16, k16, v16, total;
+  size_t dq_acc, delta, q16, do16, k16, v16, scal, total;
 };
 BwdWorkspace bwd_workspace_layout(const Plan& p);
 size_t bwd_workspace_bytes(const Plan& p, size_t* dq_acc_off, size_t* delta_off);

@@ -49,6 +49,23 @@ def assert_close(got, ref, name, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
     assert excess.max() <= 1.0 and d.mean() <= mean_abs, msg
 
 
+def assert_close_f32(got, ref, name, max_abs=MAX_ABS, mean_abs=MEAN_ABS):
+    """The same bounds for an fp32 output (the logsumexp): flat, with no widening by a bf16
+    ulp, since an fp32 value carries 24 significant bits."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), "%s has non-finite values" % name
+    d = np.abs(got - ref)
+    if d.size == 0:
+        return
+    worst = np.unravel_index(np.argmax(d), d.shape)
+    msg = "%s: max|err| %.3g at %s (got %.7g ref %.7g), mean|err| %.3g, max|ref| %.3g" % (
+        name, d[worst], worst, got[worst], ref[worst], d.mean(), np.abs(ref).max())
+    assert d.max() <= max_abs and d.mean() <= mean_abs, msg
+    return float(d.max())
+
+
 def bf16_ulp_distance(a_bits: np.ndarray, b_bits: np.ndarray) -> np.ndarray:
     """Distance in units in the last place between bf16 bit patterns (same-sign ordering)."""
     def key(b):

@@ -8,7 +8,7 @@ import torch
 import long_context_sequence_gb300 as U
 import oracle as O
 import synthetic
-from gpu_helpers import assert_close, dev_bf16, empty_bf16, host_f64
+from gpu_helpers import assert_close, assert_close_f32, dev_bf16, empty_bf16, host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +59,7 @@ def test_ring_attention_equals_causal_attention(S, P, H, G, D, std):
     n = S // P
     ro, rl = O.causal_attention(*(synthetic.bf16_to_f64(a).reshape(S, -1, D) for a in (q, k, v)))
     assert_close(host_f64(o).reshape(S, H, D), ro, "o")
-    assert_close(host_f64(lse).transpose(1, 0, 2).reshape(H, S), rl, "lse")
+    assert_close_f32(host_f64(lse).transpose(1, 0, 2).reshape(H, S), rl, "lse")
     # the exchange: every rank forwards its K and V shard P - 1 times (read + write bytes)
     assert moved == (P - 1) * P * n * G * D * 2 * 2 * 2
     assert moved == P * 2 * 2 * O.ring_volume_bytes(S, P, G, D) // 2
@@ -102,7 +102,7 @@ def test_ring_sampled_rows_8b_shape_32k():
     o_h = host_f64(o).reshape(S, H, D)
     lse_h = host_f64(lse).transpose(1, 0, 2).reshape(H, S)
     assert_close(o_h[rows], ro, "o")
-    assert_close(lse_h[:, rows], rl, "lse")
+    assert_close_f32(lse_h[:, rows], rl, "lse")
 
 
 def test_ring_empty_sequence_is_a_no_op():

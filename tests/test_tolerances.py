@@ -32,17 +32,46 @@ def _peaked_rank0(S=1024, P=4, H=8, G=4, D=128, std=3.0):
     return q, k, v, do
 
 
+def _floor_log2(m):
+    return int(np.frexp(m)[1]) - 1
+
+
+def _bwd_exponents(q, k, v, do, scale):
+    """The backward's per-call power-of-two exponents, restated from the kernels' rule:
+    2^kp scale in [2^7, 2^8); max|q'|, max|k'| in [2^7, 2^8); max|v'| in [2^-1, 2^0); edo the
+    largest exponent with 2^kp scale D max|dO'| max|v'| < 2^14 and max|dO'| < 2^15; every
+    exponent within [-60, 60] (kp within [-30, 30])."""
+    D = q.shape[-1]
+    clamp = lambda e, lim=60: int(min(max(e, -lim), lim))   # noqa: E731
+    kp = clamp(8 - int(np.frexp(scale)[1]), 30)
+    mq, mk, mv, mdo = (float(np.abs(t).max()) for t in (q, k, v, do))
+    eq = clamp(7 - _floor_log2(mq)) if mq > 0 else 0
+    ek = clamp(7 - _floor_log2(mk)) if mk > 0 else 0
+    ev = clamp(-1 - _floor_log2(mv)) if mv > 0 else 0
+    edo = 0
+    if mdo > 0:
+        edo = 14 - _floor_log2(mdo)
+        if mv > 0:
+            edo = min(edo, 13 - _floor_log2(2.0 ** kp * scale * D * mdo * mv * 2.0 ** ev))
+        edo = clamp(edo)
+    return kp, eq, ek, ev, edo
+
+
 def _simulate(q, k, v, do, p_store, ds_store):
     """The kernels' roundings on the fp64 definition:
     - forward: unnormalised P (relative to the row max) stored as bf16 for P V; the row sum
       from the unrounded P;
     - backward: O held as bf16 plus its bf16 residual for the row term D; P_s = scale * P
-      unrounded; dS = P_s (dP - D) from the unrounded P_s, stored with `ds_store` for dQ and
-      dK; P_s stored with `p_store` for dV (divided by the scale at the end);
+      unrounded; dS = P_s (dP - D) from the unrounded P_s.  Both are stored scaled by the
+      call's powers of two (P' = 2^kp P_s, dS' = 2^(kp+edo+ev) dS): dS' with `ds_store` for
+      dQ and dK, P' with `p_store` for dV, and the stored values scaled back exactly.  The
+      scaled fp16 copies of q, k, v, dO are exact (normal fp16 holds every bf16 value);
     - every output rounded once to bf16."""
     S, hl, D = q.shape
     gl = k.shape[1]
     grp, scale = hl // gl, 1.0 / np.sqrt(D)
+    kp, _, _, ev, edo = _bwd_exponents(q, k, v, do, scale)
+    f_p, f_ds = 2.0 ** kp, 2.0 ** (kp + edo + ev)
     o, lse = O.causal_attention(q, k, v)
     o_hi = _bf16(o)
     o_lo = _bf16(o - o_hi)
@@ -56,10 +85,10 @@ def _simulate(q, k, v, do, p_store, ds_store):
         o_sim[:, h] = (_bf16(pu) @ v[:, g]) / pu.sum(axis=1)[:, None]
         d_row = np.sum(do[:, h] * (o_hi[:, h] + o_lo[:, h]), axis=1)
         ps = np.where(mask, scale * np.exp(s - lse[h][:, None]), 0.0)
-        ds = ds_store(ps * (do[:, h] @ v[:, g].T - d_row[:, None]))
+        ds = ds_store(f_ds * ps * (do[:, h] @ v[:, g].T - d_row[:, None])) / f_ds
         dq[:, h] = ds @ k[:, g]
         dk[:, g] += ds.T @ q[:, h]
-        dv[:, g] += (p_store(ps).T @ do[:, h]) / scale
+        dv[:, g] += (p_store(f_p * ps).T @ do[:, h]) / (f_p * scale)
     return tuple(_bf16(t) for t in (o_sim, dq, dk, dv))
 
 
