@@ -148,9 +148,11 @@ uly_status ulysses_attn_fwd(uly_plan plan, const void *q, const void *k, const v
  * in fp16 range), with the inverse powers applied exactly to the outputs.  So gradients as
  * small as a training step's (|d_o| ~ 1e-8) keep fp16's full precision, bf16 inputs above
  * fp16's 65504 are not clipped, and scaling any input by a power of two scales the outputs
- * by exactly that factor.  Only a tensor whose largest magnitude is below 2^-53 or above
- * 2^67 (q, k, v) -- beyond the exponents' range -- cannot be fully normalised; if an fp16
- * copy would then saturate, the call reports ULY_ERR_RANGE through the status word.
+ * by exactly that factor (q and k share one exponent, q' = 2^e q and k' = 2^-e k, which
+ * balances them and leaves every logit unchanged).  Inputs that no exponent within +-60
+ * can bring into fp16's range -- in practice max|q| * max|k| >= 2^30 (logits that large
+ * leave a one-hot softmax), or max|v| or max|d_o| beyond about 2^+-60 -- would saturate
+ * an fp16 copy; the call then reports ULY_ERR_RANGE through the status word.
  * workspace: ulysses_workspace_bytes(plan) bytes of device memory (fp32 accumulators);
  * its contents on entry do not matter. */
 uly_status ulysses_attn_bwd(uly_plan plan, const void *q, const void *k, const void *v,

@@ -31,15 +31,17 @@
 // span fp32's range (a training step's dO is often 1e-5 .. 1e-8, and q, k, v may exceed
 // 65504).  So every operand is scaled by an exact power of two chosen per call from the
 // tensors' largest magnitudes (bwd_amax_kernel):
-//   q' = 2^eq q, k' = 2^ek k      largest |x'| in [2^7, 2^8)
+//   q' = 2^eq q, k' = 2^-eq k     eq balances the two: largest |q'| and |k'| at about the
+//                                 geometric mean of the two maxima (s' = q'.k' = s exactly,
+//                                 so the softmax's multiplier stays a kernel constant)
 //   v' = 2^ev v                   largest |v'| in [2^-1, 2^0)
 //   P' = 2^kp scale P             2^kp scale in [2^7, 2^8)  (kp fixed by the plan's scale)
 //   dO' = 2^edo dO                the largest edo with 2^kp scale D max|dO'| max|v'| <= 2^14
 //                                 and max|dO'| < 2^15
 // Then |dP' - D'| <= 2 D max|dO'| max|v'| and dS' = P' (dP' - D') stays below 2^15: no fp16
 // operand can overflow, and for ordinary data none is subnormal.  The outputs take the
-// inverse powers exactly (ldexp in the epilogues): dV = acc / (scale 2^(kp+edo)),
-// dK = 2^-(kp+edo+ev+eq) acc, dQ = 2^-(kp+edo+ev+ek) acc.  Scaling any input by a power of
+// inverse powers exactly (power-of-two factors in the epilogues): dV = acc / (scale
+// 2^(kp+edo)), dK = 2^-(kp+edo+ev+eq) acc, dQ = 2^-(kp+edo+ev-eq) acc.  Scaling any input by a power of
 // two therefore leaves every fp16 operand bit for bit as it was and scales the outputs
 // exactly.  A tensor whose largest magnitude lies beyond the exponents' range (|e| <= 60)
 // would saturate: the call reports ULY_ERR_RANGE through the status word.
@@ -152,7 +154,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 13);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
-  float* sl2_s = reinterpret_cast<float*>(abort_flag + 5);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int per_rank = a.gl * a.nkb;
@@ -179,8 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(drain_acc, 1);
     *abort_flag = 0;
-    // s' = q'.k' = 2^(eq+ek) q.k: the exponent's multiplier takes the inverse power
-    *sl2_s = a.scale_log2 * exp2i(-(a.exps[0] + a.exps[1]));
+
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -354,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int w2 = (warp / 4) % 2;
     const int quarter = warp % 4;
     const int row = quarter * 32 + lane;
+    const float sl2 = a.scale_log2;     // s' = q'.k' = s: the multiplier needs no scaling
     const int key_g = nb * BN + row;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t treg = tbase + lane_off + 128 * X;
@@ -413,7 +414,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             nl[i2] = f2_pack(n0, n1);
           }
         }
-        const float sl2 = *sl2_s;
         const uint64_t sc2 = f2_pack(sl2, sl2);
 #pragma unroll
         for (int i2 = 0; i2 < 8; ++i2) {
@@ -524,7 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // last block to finish) the exponents.
 // The rule, with E(m) = floor(log2 m) and every exponent clamped to [-60, 60] (so every
 // sum of two of them, and of kp, is a float exponent):
-//   eq = 7 - E(max|q|), ek = 7 - E(max|k|)     -> max|q'|, max|k'| in [2^7, 2^8)
+//   eq = floor((E(max|k|) - E(max|q|)) / 2), ek = -eq
+//                                              -> E(max|q'|) and E(max|k'|) differ by <= 1
 //   ev = -1 - E(max|v|)                        -> max|v'| in [2^-1, 2^0)
 //   edo = min(14 - E(max|dO|), 13 - E(X)), X = 2^kp scale D max|dO| max|v'|
 //                                              -> max|dO'| < 2^15 and X 2^edo < 2^14
@@ -542,8 +543,13 @@ __device__ __forceinline__ int floor_log2f(float m) {
 
 __device__ void bwd_exponents(const float (&M)[4], float scale_k, int D, int (&e)[4],
                               bool& range) {
-  e[0] = finite_pos(M[0]) ? clamp_exp(7 - floor_log2f(M[0])) : 0;
-  e[1] = finite_pos(M[1]) ? clamp_exp(7 - floor_log2f(M[1])) : 0;
+  if (finite_pos(M[0]) && finite_pos(M[1])) {
+    const int d = floor_log2f(M[1]) - floor_log2f(M[0]);
+    e[0] = clamp_exp(d >= 0 ? d / 2 : -((1 - d) / 2));   // floor(d / 2)
+  } else {
+    e[0] = 0;
+  }
+  e[1] = -e[0];
   e[2] = finite_pos(M[2]) ? clamp_exp(-1 - floor_log2f(M[2])) : 0;
   int edo = 0;
   if (finite_pos(M[3])) {

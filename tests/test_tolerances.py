@@ -38,15 +38,16 @@ def _floor_log2(m):
 
 def _bwd_exponents(q, k, v, do, scale):
     """The backward's per-call power-of-two exponents, restated from the kernels' rule:
-    2^kp scale in [2^7, 2^8); max|q'|, max|k'| in [2^7, 2^8); max|v'| in [2^-1, 2^0); edo the
-    largest exponent with 2^kp scale D max|dO'| max|v'| < 2^14 and max|dO'| < 2^15; every
-    exponent within [-60, 60] (kp within [-30, 30])."""
+    2^kp scale in [2^7, 2^8); q' = 2^eq q and k' = 2^-eq k with eq = floor((E(max|k|) -
+    E(max|q|)) / 2); max|v'| in [2^-1, 2^0); edo the largest exponent with
+    2^kp scale D max|dO'| max|v'| < 2^14 and max|dO'| < 2^15; every exponent within
+    [-60, 60] (kp within [-30, 30])."""
     D = q.shape[-1]
     clamp = lambda e, lim=60: int(min(max(e, -lim), lim))   # noqa: E731
     kp = clamp(8 - int(np.frexp(scale)[1]), 30)
     mq, mk, mv, mdo = (float(np.abs(t).max()) for t in (q, k, v, do))
-    eq = clamp(7 - _floor_log2(mq)) if mq > 0 else 0
-    ek = clamp(7 - _floor_log2(mk)) if mk > 0 else 0
+    eq = clamp((_floor_log2(mk) - _floor_log2(mq)) // 2) if mq > 0 and mk > 0 else 0
+    ek = -eq
     ev = clamp(-1 - _floor_log2(mv)) if mv > 0 else 0
     edo = 0
     if mdo > 0:
