@@ -10,8 +10,14 @@ ranks, hidden 4096, 32 query / 8 KV heads, head_dim 128, RoPE theta 500000, bf16
 Metric: causal attention fwd+bwd TFLOPS (algorithmic FLOPs: fwd 2*S^2*D*H, bwd 2.5x fwd)
 over the whole step time; the permute GB/s (read + write bytes) is reported beside it.
 
+With N > 1 GPUs (torchrun, one process per GPU) the step is the block as the pages run it
+across GPUs: P = N ranks, each holding S/N tokens, with the two all-to-alls as NCCL
+exchanges through the library (ulysses_a2a_exchange); the sequence length stays S, so the
+job's work is fixed ("strong" scaling).  --sharded runs that same path at N = 1.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
        [--seq S]    (S other than 131072 is for quick checks only)
+       [--sharded]  (the multi-GPU code path, also at N = 1)
 """
 from __future__ import annotations
 
@@ -209,6 +215,165 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def run_sharded(args, U, world, rank, local, dev, dist):
+    """One rank of a P = world GPU group: the shard's projection, the seq->head exchange of
+    q, k, v, attention of the rank's head group, the head->seq exchange of o, then the
+    backward: dO's exchange, the attention backward, and the gradients' exchange back with
+    the RoPE backward in the unpack.  Every exchange is one NCCL group (the library's)."""
+    import torch
+    w = WORKLOAD
+    S, hidden, H, G, D, theta = (args.seq or w["S"]), w["hidden"], w["H"], w["G"], w["D"], w["theta"]
+    P = world
+    cfg = U.make_config(S, P, hidden, H, G, D, rope_theta=theta)
+    plan = U.ulysses_plan_rank(cfg, rank)
+    sh = plan.shapes()
+    n = S // P
+    uid = [U.ulysses_nccl_unique_id() if rank == 0 else None]
+    if world > 1:
+        dist.broadcast_object_list(uid, src=0)
+    comm = U.ulysses_nccl_comm_init(world, rank, uid[0])
+    bf = torch.bfloat16
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    x = torch.randn(sh["x"], generator=gen, device=dev).to(bf)
+    gen2 = torch.Generator(device=dev)
+    gen2.manual_seed(999)                       # the weight is the same on every rank
+    wq = (torch.randn(sh["w"], generator=gen2, device=dev) * 0.02).to(bf)
+    do_loc = torch.randn(sh["o_seq"], generator=gen, device=dev).to(bf)
+    e = lambda name, dt=bf: torch.empty(sh[name], dtype=dt, device=dev)   # noqa: E731
+    qkv_loc = e("qkv")
+    sq, sk, sv, rq, rk, rv = e("q"), e("k"), e("v"), e("q"), e("k"), e("v")
+    o, o_lo, ro = e("o"), e("o"), e("o")
+    lse = e("lse", torch.float32)
+    o_loc = e("o_seq")
+    sdo, rdo = e("o"), e("o")
+    dq, dk, dv, xq, xk, xv = e("q"), e("k"), e("v"), e("q"), e("k"), e("v")
+    dqkv_loc = e("qkv")
+    ws = torch.empty(U.ulysses_workspace_bytes(plan), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sid = stream.cuda_stream
+    names = ["qkv_proj", "pack_qkv", "exchange_qkv", "attn_fwd", "exchange_o", "unpack_o",
+             "pack_do", "exchange_do", "attn_bwd", "exchange_grads", "unpack_grads"]
+    launches_per_step = 1 + 1 + 1 + 1 + 1 + 6 + 1   # the library's kernels (NCCL's not counted)
+
+    def step(ev=None, io=None):
+        xs, dos, os_, dqs = io if io is not None else (x, do_loc, o_loc, dqkv_loc)
+
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        U.ulysses_qkv_proj(plan, xs, wq, qkv_loc, sid)
+        mark(1)
+        U.ulysses_a2a_pack_qkv(plan, qkv_loc, sq, sk, sv, apply_rope=True, stream=sid)
+        mark(2)
+        U.ulysses_a2a_exchange(plan, comm, [sq, sk, sv], [rq, rk, rv], sid)
+        mark(3)
+        U.ulysses_attn_fwd(plan, rq, rk, rv, o, lse, sid, o_lo=o_lo)
+        mark(4)
+        U.ulysses_a2a_exchange(plan, comm, [o], [ro], sid)
+        mark(5)
+        U.ulysses_a2a_unpack_heads(plan, ro, H, os_, sid)
+        mark(6)
+        U.ulysses_a2a_pack_heads(plan, dos, H, sdo, sid)
+        mark(7)
+        U.ulysses_a2a_exchange(plan, comm, [sdo], [rdo], sid)
+        mark(8)
+        U.ulysses_attn_bwd(plan, rq, rk, rv, o, lse, rdo, dq, dk, dv, ws, sid, o_lo=o_lo)
+        mark(9)
+        U.ulysses_a2a_exchange(plan, comm, [dq, dk, dv], [xq, xk, xv], sid)
+        mark(10)
+        U.ulysses_a2a_unpack_qkv(plan, xq, xk, xv, dqs, apply_rope=True, stream=sid)
+        mark(11)
+
+    for _ in range(args.warmup):
+        step()
+    st = U.ulysses_sync_status(plan, sid)
+    if st != U.ULY_OK:
+        raise RuntimeError("device status %d during warm-up: %s" % (st, U.ulysses_last_error()))
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    st = U.ulysses_sync_status(plan, sid)
+    if st != U.ULY_OK:
+        raise RuntimeError("device status %d: %s" % (st, U.ulysses_last_error()))
+    ms_step = reduce_max_ms(t0.elapsed_time(t1) / args.steps, world, dist, dev)
+    avg = {nm: sum(e_[i].elapsed_time(e_[i + 1]) for e_ in evs) / len(evs)
+           for i, nm in enumerate(names)}
+    fwd_f, bwd_f = attn_flops(S, H, D)
+    value = job_tflops((fwd_f + bwd_f) / world, world, ms_step)
+
+    # end to end through the same calls: x and dO of the shard uploaded from pinned host
+    # memory and o and dqkv of the shard read back, every step, inside the timed region
+    hx = torch.empty(sh["x"], dtype=bf, pin_memory=True)
+    hdo = torch.empty(sh["o_seq"], dtype=bf, pin_memory=True)
+    hx.copy_(x)
+    hdo.copy_(do_loc)
+    ho = torch.empty(sh["o_seq"], dtype=bf, pin_memory=True)
+    hg = torch.empty(sh["qkv"], dtype=bf, pin_memory=True)
+    xs, dos = torch.empty_like(x), torch.empty_like(do_loc)
+
+    def e2e_step():
+        xs.copy_(hx, non_blocking=True)
+        dos.copy_(hdo, non_blocking=True)
+        step(io=(xs, dos, o_loc, dqkv_loc))
+        ho.copy_(o_loc, non_blocking=True)
+        hg.copy_(dqkv_loc, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(args.steps, 5)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ems = reduce_max_ms(e0.elapsed_time(e1) / e2e_steps, world, dist, dev)
+    if not torch.equal(hg, dqkv_loc.cpu()):
+        raise RuntimeError("e2e read-back differs from the device result")
+    e2e = {"value": job_tflops((fwd_f + bwd_f) / world, world, ems), "unit": "TFLOPS",
+           "h2d_bytes_per_step": world * (hx.numel() + hdo.numel()) * 2,
+           "d2h_bytes_per_step": world * (ho.numel() + hg.numel()) * 2, "ms_per_step": ems,
+           "copies": "on the compute stream, not overlapped", "steps": e2e_steps}
+    s2h, h2s = U.ulysses_a2a_volume(cfg)
+    if rank == 0:
+        peaks, peak_kind = load_peaks()
+        bwd_tf = bwd_f / world / (avg["attn_bwd"] * 1e-3) / 1e12
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (device torch.randn, seeded; X~N(0,1), W~N(0,0.02^2), dO~N(0,1))",
+            "config": {"workload": w["name"], "seq_len": S, "P": P, "hidden": hidden,
+                       "n_q_heads": H, "n_kv_heads": G, "head_dim": D, "rope_theta": theta,
+                       "global_batch": 1, "parallelism": "ulysses-sp%d" % P,
+                       "l2": "inputs larger than L2 (no flush)"},
+            "roofline": {"kernel": "ulysses_attn_bwd", "bound": "tensor", "achieved": bwd_tf,
+                         "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": bwd_tf / peaks["bf16_tflops_sustained"], "traffic": None,
+                         "peak_source": "%s bf16_tflops_sustained" % peak_kind},
+            "kernels_ms": avg, "exchange_bytes_per_rank": s2h + h2s,
+            "gpu_launches": launches_per_step * args.steps, "clocks": clk.summary(),
+            "e2e": e2e, "cpu_baseline": None,
+        }
+        print(json.dumps(line))
+    U.ulysses_nccl_comm_destroy(comm)
+    plan.close()
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -224,6 +389,11 @@ def run_ours(args):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if world > 1 or args.sharded:
+        run_sharded(args, U, world, rank, local, dev, dist)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     w = WORKLOAD
     S, P, hidden, H, G, D, theta = (args.seq or w["S"]), w["P"], w["hidden"], w["H"], w["G"], w["D"], w["theta"]
     plan = U.ulysses_plan(U.make_config(S, P, hidden, H, G, D, rope_theta=theta))
@@ -531,11 +701,11 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (device torch.randn, seeded; X~N(0,1), W~N(0,0.02^2), dO~N(0,1))",
             "config": {"workload": w["name"], "seq_len": S, "P": P, "hidden": hidden,
                        "n_q_heads": H, "n_kv_heads": G, "head_dim": D, "rope_theta": theta,
-                       "global_batch": world, "parallelism": "replicas" if world > 1 else "single",
+                       "global_batch": 1, "parallelism": "single GPU, P=%d virtual ranks" % P,
                        "l2": "inputs larger than L2 (no flush)"},
             "roofline": dict({"kernel": "ulysses_attn_bwd", "bound": "tensor",
                               "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
@@ -572,6 +742,8 @@ def main():
     ap.add_argument("--no-layer", action="store_true")
     ap.add_argument("--no-ring", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--sharded", action="store_true",
+                    help="run the multi-GPU (real-rank, NCCL exchange) path, also at N = 1")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.seq:
         args.warmup = 3

@@ -261,6 +261,113 @@ uly_status ulysses_ring_attn_fwd(uly_plan plan, const void *q_seq, const void *k
  * forwarded P - 1 times: (P-1) * (S/P) * 2G * D * 2. */
 uly_status ulysses_ring_volume(const uly_config *cfg, uint64_t *bytes);
 
+/* ---------------------------------------------------------------- real ranks (GPUs)
+ * The same block on P GPUs, one process (rank) per GPU, as "Snowflake's Ulysses trick
+ * ..." para 2 describes it: the two all-to-alls cross GPUs.  A rank plan describes rank
+ * `rank` of the group (cfg->P = the number of ranks): it holds the rank's token shard
+ * (n = S/P tokens from rank*n on) and, after the first exchange, the whole sequence for its
+ * head group (hl = H/P query heads, gl = G/P KV heads).  Layouts on one rank:
+ *   x_local        [n][hidden]             the shard's rows of x
+ *   qkv_local      [n][H + 2G][D]          its projection (= [n][C])
+ *   send_q         [P][n][hl][D]           block p goes to rank p: the shard's rows of rank
+ *   send_k, send_v [P][n][gl][D]           p's head group (RoPE applied at global positions)
+ *   q (received)   [P][n][hl][D]           block p came from rank p: p's shard of this head
+ *                  = [S][hl][D]            group -- in token order, the attention's layout
+ *   k, v           [S][gl][D]
+ *   o, do_head     [S][hl][D] = [P][n][hl][D]   sent as is: block p holds rank p's tokens
+ *   lse            [hl][S]                 fp32
+ *   o (received)   [P][n][hl][D]           block p came from rank p: its heads of this shard
+ *   o_local        [n][H][D]
+ * The calls that accept a rank plan:
+ *   ulysses_qkv_proj, ulysses_qkv_proj_bwd   on the shard's n rows (dw sums this rank's
+ *                     tokens only: the caller sums it over the ranks, as for any weight
+ *                     that data-parallel ranks share)
+ *   ulysses_a2a_pack_qkv, ulysses_a2a_pack_heads       write send buffers
+ *   ulysses_a2a_exchange                               the all-to-all itself
+ *   ulysses_a2a_unpack_heads, ulysses_a2a_unpack_qkv   read receive buffers
+ *   ulysses_attn_fwd, ulysses_attn_bwd, ulysses_attn_bwd_noalloc, ulysses_workspace_bytes
+ *                     the head group over all S tokens (q, k, v, o, lse as above)
+ *   ulysses_o_proj    reads o's receive buffer [P][n][hl][D] directly (no unpack)
+ *   ulysses_o_proj_bwd  writes do_head as dO's send buffer [P][n][hl][D] directly
+ * The single-GPU permutes (ulysses_seq_to_head, ulysses_seq_to_head_heads,
+ * ulysses_head_to_seq, ulysses_head_to_seq_qkv) and ring attention reject a rank plan
+ * with ULY_ERR_INVALID_ARG.  No kernel ever reads another GPU's memory: every exchange
+ * lands in the receiving rank's own buffers before any kernel reads it. */
+uly_status ulysses_plan_rank(const uly_config *cfg, int32_t rank, uly_plan *out);
+
+/* One block of an all-to-all, seen from `rank`: what it sends to `peer` and what it
+ * receives from `peer`.  Offsets and counts are in elements (D per head row). */
+typedef struct uly_a2a_block {
+  int32_t peer;
+  int32_t n_tokens;          /* tokens in the block: S/P */
+  int32_t n_heads;           /* heads in the block: n_heads/P */
+  int32_t reserved;
+  int64_t send_token_begin;  /* global index of the first token sent to peer */
+  int64_t recv_token_begin;  /* global index of the first token received from peer */
+  int32_t send_head_begin;   /* global index of the first head sent to peer */
+  int32_t recv_head_begin;   /* global index of the first head received from peer */
+  uint64_t send_offset;      /* where the block starts in the send buffer */
+  uint64_t recv_offset;      /* where the block starts in the receive buffer */
+  uint64_t count;            /* elements in the block: n_tokens * n_heads * D */
+} uly_a2a_block;
+
+/* The all-to-all's block table of `rank` (host only, no GPU needed): blocks[p] for every
+ * peer p = 0 .. P-1 (p = rank is the block a rank keeps).  to_head != 0: seq->head of a
+ * tensor of n_heads heads (H, or G for k and v): rank r sends its tokens' heads
+ * [p*n_heads/P, (p+1)*n_heads/P) to p and receives p's tokens of its own heads.  to_head
+ * == 0: head->seq, the inverse.  Both buffers are block-major ([P][n][n_heads/P][D]), so
+ * every block is one contiguous run and all blocks have the same size. */
+uly_status ulysses_a2a_table(const uly_config *cfg, int32_t rank, int32_t to_head,
+                             int32_t n_heads, uly_a2a_block *blocks);
+
+/* seq->head send buffers of a rank (rank plans only): qkv_local [n][H + 2G][D] (bf16, or
+ * fp32 when in_fp32, rounded to bf16 on the way) -> send_q [P][n][hl][D], send_k, send_v
+ * [P][n][gl][D].  apply_rope != 0 (needs rope_theta > 0) rotates q and k as
+ * ulysses_seq_to_head does, at the tokens' global positions rank*n + t. */
+uly_status ulysses_a2a_pack_qkv(uly_plan plan, const void *qkv_local, int in_fp32,
+                                int apply_rope, void *send_q, void *send_k, void *send_v,
+                                void *stream);
+
+/* seq->head send buffer of one tensor of n_heads heads (e.g. dO): x_local [n][n_heads][D]
+ * -> send [P][n][n_heads/P][D] (rank plans only). */
+uly_status ulysses_a2a_pack_heads(uly_plan plan, const void *x_local, int n_heads, void *send,
+                                  void *stream);
+
+/* head->seq receive buffer of one tensor of n_heads heads (e.g. o): recv
+ * [P][n][n_heads/P][D] -> x_local [n][n_heads][D] (rank plans only). */
+uly_status ulysses_a2a_unpack_heads(uly_plan plan, const void *recv, int n_heads,
+                                    void *x_local, void *stream);
+
+/* head->seq receive buffers of the attention gradients (rank plans only): recv_dq
+ * [P][n][hl][D], recv_dk, recv_dv [P][n][gl][D] -> dqkv_local [n][H + 2G][D], with the RoPE
+ * backward on the q and k parts at the global positions when apply_rope != 0, as
+ * ulysses_head_to_seq_qkv does. */
+uly_status ulysses_a2a_unpack_qkv(uly_plan plan, const void *recv_dq, const void *recv_dk,
+                                  const void *recv_dv, int apply_rope, void *dqkv_local,
+                                  void *stream);
+
+/* The all-to-all between the ranks of a rank plan's group, over NCCL (the library loads
+ * libnccl.so.2 when first needed; ULY_ERR_UNSUPPORTED if it cannot).  For each of the
+ * n_buffers (1..8) buffer pairs, rank r sends bytes_per_peer[i] bytes from
+ * send[i] + p * bytes_per_peer[i] to every rank p and receives p's block into
+ * recv[i] + p * bytes_per_peer[i] -- the block-major layout of ulysses_a2a_table.  All
+ * sends and receives form one NCCL group, enqueued on `stream`.  comm must be an NCCL
+ * communicator (ncclComm_t) of exactly the plan's P ranks in which this process is rank
+ * `rank` (ulysses_nccl_comm_init makes one).  Send and receive buffers are device memory
+ * of this GPU and must not overlap. */
+uly_status ulysses_a2a_exchange(uly_plan plan, void *comm, int32_t n_buffers,
+                                const void *const *send, void *const *recv,
+                                const uint64_t *bytes_per_peer, void *stream);
+
+/* NCCL set-up for ulysses_a2a_exchange, so that a plain C caller needs no NCCL header:
+ * one rank draws the 128-byte id, every rank receives it (by any channel) and joins with
+ * its rank.  ulysses_nccl_comm_init must be called by all nranks processes, each with its
+ * own GPU current; it blocks until all have joined. */
+uly_status ulysses_nccl_unique_id(uint8_t id[128]);
+uly_status ulysses_nccl_comm_init(int32_t nranks, int32_t rank, const uint8_t id[128],
+                                  void **comm);
+uly_status ulysses_nccl_comm_destroy(void *comm);
+
 /* Description of the last error on this thread ("" if none). */
 const char *ulysses_last_error(void);
 

@@ -28,7 +28,10 @@ EXPORTED = ("ulysses_plan", "ulysses_plan_destroy", "ulysses_workspace_bytes",
             "ulysses_o_proj", "ulysses_o_proj_bwd", "ulysses_ring_workspace_bytes",
             "ulysses_ring_attn_fwd", "ulysses_ring_volume",
             "ulysses_sync_status", "ulysses_bytes_moved", "ulysses_a2a_volume",
-            "ulysses_last_error")
+            "ulysses_last_error", "ulysses_plan_rank", "ulysses_a2a_table",
+            "ulysses_a2a_pack_qkv", "ulysses_a2a_pack_heads", "ulysses_a2a_unpack_heads",
+            "ulysses_a2a_unpack_qkv", "ulysses_a2a_exchange", "ulysses_nccl_unique_id",
+            "ulysses_nccl_comm_init", "ulysses_nccl_comm_destroy")
 
 
 class UlyssesError(RuntimeError):
@@ -45,6 +48,16 @@ class UlyConfig(ctypes.Structure):
                 ("causal", ctypes.c_int32), ("wait_timeout_ms", ctypes.c_int32),
                 ("softmax_scale", ctypes.c_double), ("rope_theta", ctypes.c_double),
                 ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+class A2ABlock(ctypes.Structure):
+    """Mirror of struct uly_a2a_block."""
+    _fields_ = [("peer", ctypes.c_int32), ("n_tokens", ctypes.c_int32),
+                ("n_heads", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("send_token_begin", ctypes.c_int64), ("recv_token_begin", ctypes.c_int64),
+                ("send_head_begin", ctypes.c_int32), ("recv_head_begin", ctypes.c_int32),
+                ("send_offset", ctypes.c_uint64), ("recv_offset", ctypes.c_uint64),
+                ("count", ctypes.c_uint64)]
 
 
 def make_config(seq_len, P, hidden, n_q_heads, n_kv_heads, head_dim, rope_theta=0.0,
@@ -91,6 +104,19 @@ def load_library(path: str = LIB_PATH):
         "ulysses_a2a_volume": ([ctypes.POINTER(UlyConfig), ctypes.POINTER(u64),
                                 ctypes.POINTER(u64)], i32),
         "ulysses_last_error": ([], ctypes.c_char_p),
+        "ulysses_plan_rank": ([ctypes.POINTER(UlyConfig), ctypes.c_int32, ctypes.POINTER(vp)], i32),
+        "ulysses_a2a_table": ([ctypes.POINTER(UlyConfig), ctypes.c_int32, ctypes.c_int32,
+                               ctypes.c_int32, ctypes.POINTER(A2ABlock)], i32),
+        "ulysses_a2a_pack_qkv": ([vp, vp, i32, i32, vp, vp, vp, vp], i32),
+        "ulysses_a2a_pack_heads": ([vp, vp, i32, vp, vp], i32),
+        "ulysses_a2a_unpack_heads": ([vp, vp, i32, vp, vp], i32),
+        "ulysses_a2a_unpack_qkv": ([vp, vp, vp, vp, i32, vp, vp], i32),
+        "ulysses_a2a_exchange": ([vp, vp, ctypes.c_int32, ctypes.POINTER(vp), ctypes.POINTER(vp),
+                                  ctypes.POINTER(u64), vp], i32),
+        "ulysses_nccl_unique_id": ([ctypes.POINTER(ctypes.c_uint8)], i32),
+        "ulysses_nccl_comm_init": ([ctypes.c_int32, ctypes.c_int32,
+                                    ctypes.POINTER(ctypes.c_uint8), ctypes.POINTER(vp)], i32),
+        "ulysses_nccl_comm_destroy": ([vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -127,11 +153,12 @@ def _stream(stream):
 
 
 class Plan:
-    """Owns a uly_plan handle."""
+    """Owns a uly_plan handle (rank is None for the single-GPU virtual ranks)."""
 
-    def __init__(self, handle: int, cfg: UlyConfig):
+    def __init__(self, handle: int, cfg: UlyConfig, rank=None):
         self.handle = handle
         self.cfg = cfg
+        self.rank = rank
 
     def close(self):
         if self.handle:
@@ -148,6 +175,12 @@ class Plan:
     def shapes(self):
         c = self.cfg
         S, P, H, G, D = c.seq_len, c.P, c.n_q_heads, c.n_kv_heads, c.head_dim
+        if self.rank is not None:       # one real rank: its shard and its head group
+            n, hl, gl = S // P, H // P, G // P
+            return {"x": (n, c.hidden), "w": ((H + 2 * G) * D, c.hidden),
+                    "qkv": (n, H + 2 * G, D), "q": (P, n, hl, D), "k": (P, n, gl, D),
+                    "v": (P, n, gl, D), "o": (P, n, hl, D), "lse": (hl, S),
+                    "o_seq": (n, H, D)}
         return {"x": (S, c.hidden), "w": ((H + 2 * G) * D, c.hidden),
                 "qkv": (P, S // P, H + 2 * G, D), "q": (P, S, H // P, D),
                 "k": (P, S, G // P, D), "v": (P, S, G // P, D), "o": (P, S, H // P, D),
@@ -159,6 +192,82 @@ def ulysses_plan(cfg: UlyConfig) -> Plan:
     h = ctypes.c_void_p()
     _check(load_library().ulysses_plan(ctypes.byref(cfg), ctypes.byref(h)))
     return Plan(h.value, cfg)
+
+
+def ulysses_plan_rank(cfg: UlyConfig, rank: int) -> Plan:
+    """Plan of one real rank of a cfg.P-GPU group."""
+    h = ctypes.c_void_p()
+    _check(load_library().ulysses_plan_rank(ctypes.byref(cfg), int(rank), ctypes.byref(h)))
+    return Plan(h.value, cfg, rank=int(rank))
+
+
+def ulysses_a2a_table(cfg: UlyConfig, rank: int, to_head: bool, n_heads: int):
+    """The all-to-all block table of `rank` (host only): one dict per peer."""
+    blocks = (A2ABlock * cfg.P)()
+    _check(load_library().ulysses_a2a_table(ctypes.byref(cfg), int(rank), 1 if to_head else 0,
+                                            int(n_heads), blocks))
+    return [{f: getattr(b, f) for f, _ in A2ABlock._fields_ if f != "reserved"} for b in blocks]
+
+
+def ulysses_a2a_pack_qkv(plan, qkv_local, send_q, send_k, send_v, apply_rope=False,
+                         stream=None):
+    import torch
+    in_fp32 = 1 if qkv_local.dtype == torch.float32 else 0
+    _check(load_library().ulysses_a2a_pack_qkv(plan.handle, _ptr(qkv_local), in_fp32,
+                                               1 if apply_rope else 0, _ptr(send_q),
+                                               _ptr(send_k), _ptr(send_v), _stream(stream)))
+
+
+def ulysses_a2a_pack_heads(plan, x_local, n_heads, send, stream=None):
+    _check(load_library().ulysses_a2a_pack_heads(plan.handle, _ptr(x_local), int(n_heads),
+                                                 _ptr(send), _stream(stream)))
+
+
+def ulysses_a2a_unpack_heads(plan, recv, n_heads, x_local, stream=None):
+    _check(load_library().ulysses_a2a_unpack_heads(plan.handle, _ptr(recv), int(n_heads),
+                                                   _ptr(x_local), _stream(stream)))
+
+
+def ulysses_a2a_unpack_qkv(plan, recv_dq, recv_dk, recv_dv, dqkv_local, apply_rope=False,
+                           stream=None):
+    _check(load_library().ulysses_a2a_unpack_qkv(plan.handle, _ptr(recv_dq), _ptr(recv_dk),
+                                                 _ptr(recv_dv), 1 if apply_rope else 0,
+                                                 _ptr(dqkv_local), _stream(stream)))
+
+
+def ulysses_a2a_exchange(plan, comm, sends, recvs, stream=None):
+    """The all-to-all of block-major buffers (one NCCL group over all pairs)."""
+    n = len(sends)
+    if n != len(recvs) or n == 0:
+        raise ValueError("need as many receive buffers as send buffers")
+    for a, b in zip(sends, recvs):
+        if a.nbytes != b.nbytes or a.nbytes % plan.cfg.P:
+            raise ValueError("send and receive buffers must have equal sizes divisible by P")
+    sp = (ctypes.c_void_p * n)(*[_ptr(t) for t in sends])
+    rp = (ctypes.c_void_p * n)(*[_ptr(t) for t in recvs])
+    bp = (ctypes.c_uint64 * n)(*[t.nbytes // plan.cfg.P for t in sends])
+    _check(load_library().ulysses_a2a_exchange(plan.handle, comm, n, sp, rp, bp,
+                                               _stream(stream)))
+
+
+def ulysses_nccl_unique_id() -> bytes:
+    buf = (ctypes.c_uint8 * 128)()
+    _check(load_library().ulysses_nccl_unique_id(buf))
+    return bytes(buf)
+
+
+def ulysses_nccl_comm_init(nranks: int, rank: int, uid: bytes) -> int:
+    """Joins an NCCL communicator (all nranks processes call it, each on its own GPU)."""
+    if len(uid) != 128:
+        raise ValueError("the NCCL id has 128 bytes")
+    buf = (ctypes.c_uint8 * 128)(*uid)
+    comm = ctypes.c_void_p()
+    _check(load_library().ulysses_nccl_comm_init(int(nranks), int(rank), buf, ctypes.byref(comm)))
+    return comm.value
+
+
+def ulysses_nccl_comm_destroy(comm: int):
+    _check(load_library().ulysses_nccl_comm_destroy(comm))
 
 
 def ulysses_plan_destroy(plan: Plan):

@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)
     if relink:
         tmp = LIB + ".tmp%d" % os.getpid()
-        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))

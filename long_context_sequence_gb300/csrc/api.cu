@@ -104,6 +104,29 @@ bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims_in[
   return true;
 }
 
+void make_view(const Plan& src, Plan& dst, int64_t S, int P, int H, int G) {
+  dst.cfg = src.cfg;
+  dst.cfg.seq_len = S;
+  dst.cfg.P = P;
+  dst.cfg.n_q_heads = H;
+  dst.cfg.n_kv_heads = G;
+  dst.device = src.device;
+  dst.rank = -1;
+  dst.S = S;
+  dst.P = P;
+  dst.hidden = src.hidden;
+  dst.H = H;
+  dst.G = G;
+  dst.D = src.D;
+  dst.scale = src.scale;
+  dst.rope_hi = src.rope_hi;
+  dst.rope_lo = src.rope_lo;
+  dst.status = src.status;
+  dst.limit_ns = src.limit_ns;
+  dst.noalloc_scratch = src.noalloc_scratch;
+  dst.noalloc_setup_error = src.noalloc_setup_error;
+}
+
 uly_status set_error(uly_status s, const char* msg) {
   if (s == ULY_OK) {
     g_err[0] = 0;
@@ -196,15 +219,20 @@ uly_status launched(cudaError_t e, const char* what) {
   return ULY_OK;
 }
 
-}  // namespace
+uly_status reject_rank_plan(uly_plan plan, const char* what) {
+  return fail(ULY_ERR_INVALID_ARG,
+              "%s works on the single-GPU virtual ranks; a rank plan (rank %d) exchanges "
+              "through ulysses_a2a_pack_* / ulysses_a2a_exchange / ulysses_a2a_unpack_*",
+              what, plan->p.rank);
+}
 
-extern "C" {
-
-uly_status ulysses_plan(const uly_config* cfg, uly_plan* out) {
+uly_status make_plan(const uly_config* cfg, int32_t rank, uly_plan* out) {
   if (!out) return fail(ULY_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   uly_status s = validate(cfg);
   if (s != ULY_OK) return s;
+  if (rank < -1 || rank >= cfg->P)
+    return fail(ULY_ERR_INVALID_ARG, "rank %d outside [0, P = %d)", rank, cfg->P);
   uly_plan h = new (std::nothrow) uly_plan_s;
   if (!h) return fail(ULY_ERR_OOM, "host allocation failed");
   Plan& p = h->p;
@@ -242,9 +270,25 @@ uly_status ulysses_plan(const uly_config* cfg, uly_plan* out) {
   // ulysses_attn_bwd_noalloc ever loads device code or allocates.  A failure only disables
   // that entry point (it reports the error); the rest of the plan works without it.
   uly::noalloc_setup(p);
+  if (rank >= 0) {
+    p.rank = rank;
+    uly::make_view(p, h->heads, p.S, 1, p.H / p.P, p.G / p.P);
+    uly::make_view(p, h->shard, p.S / p.P, p.P, p.H, p.G);
+  }
   *out = h;
   uly::g_err[0] = 0;
   return ULY_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+uly_status ulysses_plan(const uly_config* cfg, uly_plan* out) { return make_plan(cfg, -1, out); }
+
+uly_status ulysses_plan_rank(const uly_config* cfg, int32_t rank, uly_plan* out) {
+  if (rank < 0) return fail(ULY_ERR_INVALID_ARG, "rank must be >= 0 (got %d)", rank);
+  return make_plan(cfg, rank, out);
 }
 
 uly_status ulysses_plan_destroy(uly_plan plan) {
@@ -256,13 +300,13 @@ uly_status ulysses_plan_destroy(uly_plan plan) {
 
 size_t ulysses_workspace_bytes(uly_plan plan) {
   if (!plan) return 0;
-  return uly::bwd_workspace_bytes(plan->p, nullptr, nullptr);
+  return uly::bwd_workspace_bytes(uly::attn_view(plan), nullptr, nullptr);
 }
 
 uly_status ulysses_qkv_proj(uly_plan plan, const void* x, const void* w, void* qkv,
                             void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
   if (!x || !w || !qkv) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(x) || !aligned16(w) || !aligned16(qkv))
@@ -275,6 +319,7 @@ uly_status ulysses_qkv_proj(uly_plan plan, const void* x, const void* w, void* q
 uly_status ulysses_seq_to_head(uly_plan plan, const void* qkv_seq, int in_fp32, int apply_rope,
                                void* q, void* k, void* v, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->p.rank >= 0) return reject_rank_plan(plan, "ulysses_seq_to_head");
   Plan& p = plan->p;
   if (p.S == 0) return ULY_OK;
   if (!qkv_seq || !q || !k || !v) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -292,6 +337,8 @@ uly_status ulysses_seq_to_head(uly_plan plan, const void* qkv_seq, int in_fp32, 
 static uly_status permute_heads(uly_plan plan, const void* in, int n_heads, void* out,
                                 bool to_head, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->p.rank >= 0)
+    return reject_rank_plan(plan, to_head ? "ulysses_seq_to_head_heads" : "ulysses_head_to_seq");
   Plan& p = plan->p;
   if (n_heads != p.H && n_heads != p.G)
     return fail(ULY_ERR_INVALID_ARG, "n_heads must be n_q_heads or n_kv_heads (got %d)", n_heads);
@@ -317,7 +364,7 @@ uly_status ulysses_head_to_seq(uly_plan plan, const void* x_head, int n_heads, v
 uly_status ulysses_attn_fwd(uly_plan plan, const void* q, const void* k, const void* v, void* o,
                             void* o_lo, float* lse, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = uly::attn_view(plan);
   if (p.S == 0) return ULY_OK;
   if (!q || !k || !v || !o || !lse) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
@@ -331,7 +378,7 @@ uly_status ulysses_attn_bwd(uly_plan plan, const void* q, const void* k, const v
                             const void* o, const void* o_lo, const float* lse, const void* d_o,
                             void* dq, void* dk, void* dv, void* workspace, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = uly::attn_view(plan);
   if (p.S == 0) return ULY_OK;
   if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv || !workspace)
     return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -346,6 +393,7 @@ uly_status ulysses_attn_bwd(uly_plan plan, const void* q, const void* k, const v
 uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void* dq, const void* dk, const void* dv,
                                    int apply_rope, void* dqkv_seq, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->p.rank >= 0) return reject_rank_plan(plan, "ulysses_head_to_seq_qkv");
   Plan& p = plan->p;
   if (p.S == 0) return ULY_OK;
   if (!dq || !dk || !dv || !dqkv_seq) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -362,7 +410,7 @@ uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void* dq, const void* dk
 uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void* x, const void* w, const void* dqkv,
                                 void* dx, float* dw, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
   if (!x || !w || !dqkv) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(x) || !aligned16(w) || !aligned16(dqkv) || !aligned16(dx) || !aligned16(dw))
@@ -375,7 +423,7 @@ uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void* x, const void* w, con
 uly_status ulysses_o_proj(uly_plan plan, const void* o_head, const void* wo, void* y,
                           void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
   if (!o_head || !wo || !y) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(o_head) || !aligned16(wo) || !aligned16(y))
@@ -387,7 +435,7 @@ uly_status ulysses_o_proj(uly_plan plan, const void* o_head, const void* wo, voi
 uly_status ulysses_o_proj_bwd(uly_plan plan, const void* o_head, const void* wo, const void* dy,
                               void* do_head, float* dwo, void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
   if (!o_head || !wo || !dy) return fail(ULY_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(o_head) || !aligned16(wo) || !aligned16(dy) || !aligned16(do_head) ||
@@ -442,6 +490,7 @@ uly_status ulysses_ring_attn_fwd(uly_plan plan, const void* q_seq, const void* k
                                  const void* v_seq, void* o_seq, float* lse, void* workspace,
                                  void* stream) {
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
+  if (plan->p.rank >= 0) return reject_rank_plan(plan, "ulysses_ring_attn_fwd");
   Plan& p = plan->p;
   if (p.S == 0) return ULY_OK;
   if (!q_seq || !k_seq || !v_seq || !o_seq || !lse || !workspace)

@@ -61,7 +61,7 @@ extern "C" uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void* q, con
                                                void* dk, void* dv, void* stream) {
   using namespace uly;
   if (!plan) return set_error(ULY_ERR_INVALID_ARG, "plan is NULL");
-  const Plan& p = plan->p;
+  const Plan& p = attn_view(plan);
   if (p.S == 0) return set_error(ULY_OK, "");
   if (!q || !k || !v || !o || !lse || !d_o || !dq || !dk || !dv)
     return set_error(ULY_ERR_INVALID_ARG, "NULL tensor pointer");

@@ -9,6 +9,11 @@
 // sides stay coalesced.  The memory-bound roofline is read + write bytes / HBM bandwidth.
 // The q/k/v kernels, which may apply RoPE, give each thread one 8-pair chunk of one token
 // across all its heads, so the token's angles are built once, not once per head.
+//
+// The same kernels serve one real rank of a multi-GPU group: run over the rank's own S/P
+// tokens (S := S/P) with the RoPE positions offset by the shard's first global token
+// (pos0), seq->head writes the P per-peer send blocks [P][S/P][heads/P][D] of an
+// all-to-all, and head->seq turns the P received blocks back into the shard's rows.
 #include <cuda_bf16.h>
 
 #include "ptx.cuh"
@@ -108,7 +113,8 @@ __device__ __forceinline__ TokenChunk token_chunk(int64_t b, int upr, int64_t S)
 template <bool kFp32In, bool kRope>
 __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
     const void* __restrict__ in, __nv_bfloat16* __restrict__ q, __nv_bfloat16* __restrict__ k,
-    __nv_bfloat16* __restrict__ v, int64_t S, int P, int H, int G, int D, RopeTab rope) {
+    __nv_bfloat16* __restrict__ v, int64_t S, int P, int H, int G, int D, RopeTab rope,
+    int64_t pos0) {
   const int C = H + 2 * G;
   const int upr = D / 16;
   const int hq = H / P, hk = G / P;
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
     const int64_t s = tc.s;
     const int e_lo = tc.cu * 8, e_hi = D / 2 + tc.cu * 8;
     float cs[8], sn[8];
-    if (kRope) rope_angles8(rope, s, e_lo, cs, sn);
+    if (kRope) rope_angles8(rope, pos0 + s, e_lo, cs, sn);
     const char* row = reinterpret_cast<const char*>(in) + (size_t)s * C * D * esz;
 #pragma unroll 2
     for (int c = 0; c < C; ++c) {
@@ -167,7 +173,7 @@ template <bool kRope>
 __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
     const __nv_bfloat16* __restrict__ dq, const __nv_bfloat16* __restrict__ dk,
     const __nv_bfloat16* __restrict__ dv, __nv_bfloat16* __restrict__ out, int64_t S, int P,
-    int H, int G, int D, RopeTab rope) {
+    int H, int G, int D, RopeTab rope, int64_t pos0) {
   const int C = H + 2 * G;
   const int upr = D / 16;
   const int hq = H / P, hk = G / P;
@@ -178,7 +184,7 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
     const int64_t s = tc.s;
     const int e_lo = tc.cu * 8, e_hi = D / 2 + tc.cu * 8;
     float cs[8], sn[8];
-    if (kRope) rope_angles8(rope, s, e_lo, cs, sn);
+    if (kRope) rope_angles8(rope, pos0 + s, e_lo, cs, sn);
     __nv_bfloat16* row = out + (size_t)s * C * D;
 #pragma unroll 2
     for (int c = 0; c < C; ++c) {
@@ -263,25 +269,26 @@ int token_chunk_grid(const Plan& p, int64_t S) {
 }  // namespace
 
 cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool rope, void* q,
-                               void* k, void* v, cudaStream_t st) {
+                               void* k, void* v, cudaStream_t st, int64_t pos0) {
   const int grid = token_chunk_grid(p, p.S);
   RopeTab tab{p.rope_hi, p.rope_lo, p.D / 2};
   auto* qb = static_cast<__nv_bfloat16*>(q);
   auto* kb = static_cast<__nv_bfloat16*>(k);
   auto* vb = static_cast<__nv_bfloat16*>(v);
   if (in_fp32 && rope)
-    seq_to_head_kernel<true, true><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab);
+    seq_to_head_kernel<true, true><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab, pos0);
   else if (in_fp32)
-    seq_to_head_kernel<true, false><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab);
+    seq_to_head_kernel<true, false><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab, pos0);
   else if (rope)
-    seq_to_head_kernel<false, true><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab);
+    seq_to_head_kernel<false, true><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab, pos0);
   else
-    seq_to_head_kernel<false, false><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab);
+    seq_to_head_kernel<false, false><<<grid, kThreads, 0, st>>>(in, qb, kb, vb, p.S, p.P, p.H, p.G, p.D, tab, pos0);
   return cudaGetLastError();
 }
 
 cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk,
-                                   const void* dv, bool rope, void* out, cudaStream_t st) {
+                                   const void* dv, bool rope, void* out, cudaStream_t st,
+                                   int64_t pos0) {
   const int grid = token_chunk_grid(p, p.S);
   RopeTab tab{p.rope_hi, p.rope_lo, p.D / 2};
   auto* a = static_cast<const __nv_bfloat16*>(dq);
@@ -289,9 +296,9 @@ cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk
   auto* c = static_cast<const __nv_bfloat16*>(dv);
   auto* o = static_cast<__nv_bfloat16*>(out);
   if (rope)
-    head_to_seq_qkv_kernel<true><<<grid, kThreads, 0, st>>>(a, b, c, o, p.S, p.P, p.H, p.G, p.D, tab);
+    head_to_seq_qkv_kernel<true><<<grid, kThreads, 0, st>>>(a, b, c, o, p.S, p.P, p.H, p.G, p.D, tab, pos0);
   else
-    head_to_seq_qkv_kernel<false><<<grid, kThreads, 0, st>>>(a, b, c, o, p.S, p.P, p.H, p.G, p.D, tab);
+    head_to_seq_qkv_kernel<false><<<grid, kThreads, 0, st>>>(a, b, c, o, p.S, p.P, p.H, p.G, p.D, tab, pos0);
   return cudaGetLastError();
 }
 

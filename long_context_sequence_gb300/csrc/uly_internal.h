@@ -19,6 +19,7 @@ constexpr int kRopeL = 1024;
 struct Plan {
   uly_config cfg;
   int device = 0;
+  int rank = -1;               // >= 0: one real rank of a P-GPU group (ulysses_plan_rank)
   int64_t S = 0;
   int P = 1, hidden = 0, H = 0, G = 0, D = 0;
   float scale = 0.f;
@@ -40,12 +41,14 @@ cudaError_t noalloc_setup(Plan& p);
 uly_status set_error(uly_status s, const char* msg);
 
 // Launchers: each validates nothing (api.cu did) and returns the launch error.
+// pos0: global position of the first token (RoPE); 0 but for one real rank's shard.
 cudaError_t launch_seq_to_head(const Plan& p, const void* in, bool in_fp32, bool rope, void* q,
-                               void* k, void* v, cudaStream_t st);
+                               void* k, void* v, cudaStream_t st, int64_t pos0 = 0);
 cudaError_t launch_permute_heads(const Plan& p, const void* in, int n_heads, void* out,
                                  bool to_head, cudaStream_t st);
 cudaError_t launch_head_to_seq_qkv(const Plan& p, const void* dq, const void* dk,
-                                   const void* dv, bool rope, void* out, cudaStream_t st);
+                                   const void* dv, bool rope, void* out, cudaStream_t st,
+                                   int64_t pos0 = 0);
 cudaError_t launch_qkv_gemm(const Plan& p, const void* x, const void* w, void* out,
                             cudaStream_t st);
 // y = o wo^T with o read in the head layout (bf16 [S][hidden]).
@@ -98,9 +101,22 @@ bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4],
 
 int num_sms(int device);
 
+// Copies p's shared state into a view of other sizes (same device, tables, status word).
+void make_view(const Plan& src, Plan& dst, int64_t S, int P, int H, int G);
+
 }  // namespace uly
 
-// The opaque handle of the C ABI.
+// The opaque handle of the C ABI.  For a rank plan, `heads` is the rank's head group over
+// all S tokens as a one-rank plan (attention), `shard` its S/P tokens with the group's P
+// ranks (projections, pack and unpack of the exchanges).
 struct uly_plan_s {
   uly::Plan p;
+  uly::Plan heads;
+  uly::Plan shard;
 };
+
+namespace uly {
+// The view an entry point works on.
+inline const Plan& attn_view(const uly_plan_s* h) { return h->p.rank >= 0 ? h->heads : h->p; }
+inline const Plan& rows_view(const uly_plan_s* h) { return h->p.rank >= 0 ? h->shard : h->p; }
+}  // namespace uly

@@ -111,3 +111,27 @@ def test_missing_library_fails_loudly(tmp_path):
                          cwd=ROOT, timeout=120)
     assert out.returncode == 0, out.stderr
     assert out.stdout.strip() == "3"
+
+
+def test_a2a_table_host_only(lib):
+    """The block table of a rank (no GPU): P equal contiguous blocks, block-major in both
+    buffers; seq->head sends the rank's tokens of every peer's heads, head->seq the inverse."""
+    cfg = U.make_config(seq_len=4096, P=8, hidden=4096, n_q_heads=32, n_kv_heads=8, head_dim=128)
+    n = 4096 // 8
+    for rank in (0, 3, 7):
+        t = U.ulysses_a2a_table(cfg, rank, True, 32)
+        assert [b["peer"] for b in t] == list(range(8))
+        assert all(b["count"] == n * 4 * 128 and b["send_offset"] == b["peer"] * b["count"] ==
+                   b["recv_offset"] for b in t)
+        assert all(b["send_token_begin"] == rank * n and b["send_head_begin"] == 4 * b["peer"] and
+                   b["recv_token_begin"] == b["peer"] * n and b["recv_head_begin"] == 4 * rank
+                   for b in t)
+        back = U.ulysses_a2a_table(cfg, rank, False, 8)
+        assert all(b["send_token_begin"] == b["peer"] * n and b["send_head_begin"] == rank and
+                   b["recv_token_begin"] == rank * n and b["recv_head_begin"] == b["peer"]
+                   for b in back)
+    for bad in (dict(rank=8, to_head=True, n_heads=32), dict(rank=-1, to_head=True, n_heads=32),
+                dict(rank=0, to_head=False, n_heads=16)):
+        with pytest.raises(U.UlyssesError) as ei:
+            U.ulysses_a2a_table(cfg, **bad)
+        assert ei.value.status == U.ULY_ERR_INVALID_ARG
