@@ -64,8 +64,11 @@ typedef enum uly_status {
   ULY_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed */
   ULY_ERR_OOM = 4,          /* the plan could not allocate its own small buffers */
   ULY_ERR_TIMEOUT = 5,      /* a device-side wait ran past its limit (from sync_status) */
-  ULY_ERR_RANGE = 6         /* an input's magnitude lies beyond what the backward's scaled
+  ULY_ERR_RANGE = 6,        /* an input's magnitude lies beyond what the backward's scaled
                                fp16 operands can hold (from sync_status) */
+  ULY_ERR_BOUNDS = 7        /* debug build (libulysses_debug.so) only: a kernel computed a
+                               global index outside its buffer and skipped the access (from
+                               sync_status) */
 } uly_status;
 
 /* Plan flags. */

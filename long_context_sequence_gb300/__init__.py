@@ -12,14 +12,18 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libulysses.so")
+# ULY_LIBRARY=debug selects the bounds-checking debug build (libulysses_debug.so); any other
+# value is taken as the library's path.
+_CHOICE = os.environ.get("ULY_LIBRARY", "")
+LIB_PATH = (os.path.join(_HERE, "libulysses_debug.so") if _CHOICE == "debug"
+            else _CHOICE or os.path.join(_HERE, "libulysses.so"))
 
 (ULY_OK, ULY_ERR_INVALID_ARG, ULY_ERR_UNSUPPORTED, ULY_ERR_CUDA, ULY_ERR_OOM, ULY_ERR_TIMEOUT,
- ULY_ERR_RANGE) = range(7)
+ ULY_ERR_RANGE, ULY_ERR_BOUNDS) = range(8)
 ULY_FLAG_INJECT_STALL = 0x1
 _STATUS_NAMES = {0: "ULY_OK", 1: "ULY_ERR_INVALID_ARG", 2: "ULY_ERR_UNSUPPORTED",
                  3: "ULY_ERR_CUDA", 4: "ULY_ERR_OOM", 5: "ULY_ERR_TIMEOUT",
-                 6: "ULY_ERR_RANGE"}
+                 6: "ULY_ERR_RANGE", 7: "ULY_ERR_BOUNDS"}
 
 EXPORTED = ("ulysses_plan", "ulysses_plan_destroy", "ulysses_workspace_bytes",
             "ulysses_qkv_proj", "ulysses_seq_to_head", "ulysses_seq_to_head_heads",

@@ -17,6 +17,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libulysses.so")
+# the debug build (-DULY_DEBUG): kernels bounds-check every global index they compute
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libulysses_debug.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
               "--expt-relaxed-constexpr", "-I", os.path.join(ROOT, "include")]
@@ -34,8 +37,10 @@ def _headers():
         [os.path.join(ROOT, "include", "ulysses.h")]
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link; returns the path of libulysses.so."""
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile and link; returns the path of libulysses.so (libulysses_debug.so when debug)."""
+    BUILD, LIB = (BUILD_DEBUG, LIB_DEBUG) if debug else (globals()["BUILD"], globals()["LIB"])
+    flags = NVCC_FLAGS + (["-DULY_DEBUG"] if debug else [])
     os.makedirs(BUILD, exist_ok=True)
     nvcc = _nvcc()
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
@@ -52,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         if not stale:
             return src, ""
         tmp = obj + ".tmp%d" % os.getpid()
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", tmp]
+        cmd = [nvcc, *ARCH, *flags, "-c", src, "-o", tmp]
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s%s" % (src, res.stdout, res.stderr))
@@ -78,6 +83,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+def build_both(force: bool = False) -> str:
+    """The release and the debug library, compiled together (one pool of nvcc processes)."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        rel = ex.submit(build, force)
+        dbg = ex.submit(build, force, False, True)
+        dbg.result()
+        return rel.result()
+
+
 if __name__ == "__main__":
     import sys
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -284,9 +284,13 @@ uly_status make_plan(const uly_config* cfg, int32_t rank, uly_plan* out) {
 
 extern "C" {
 
-uly_status ulysses_plan(const uly_config* cfg, uly_plan* out) { return make_plan(cfg, -1, out); }
+uly_status ulysses_plan(const uly_config* cfg, uly_plan* out) {
+  ULY_CALL_RANGE();
+  return make_plan(cfg, -1, out);
+}
 
 uly_status ulysses_plan_rank(const uly_config* cfg, int32_t rank, uly_plan* out) {
+  ULY_CALL_RANGE();
   if (rank < 0) return fail(ULY_ERR_INVALID_ARG, "rank must be >= 0 (got %d)", rank);
   return make_plan(cfg, rank, out);
 }
@@ -305,6 +309,7 @@ size_t ulysses_workspace_bytes(uly_plan plan) {
 
 uly_status ulysses_qkv_proj(uly_plan plan, const void* x, const void* w, void* qkv,
                             void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
@@ -318,6 +323,7 @@ uly_status ulysses_qkv_proj(uly_plan plan, const void* x, const void* w, void* q
 
 uly_status ulysses_seq_to_head(uly_plan plan, const void* qkv_seq, int in_fp32, int apply_rope,
                                void* q, void* k, void* v, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   if (plan->p.rank >= 0) return reject_rank_plan(plan, "ulysses_seq_to_head");
   Plan& p = plan->p;
@@ -353,16 +359,19 @@ static uly_status permute_heads(uly_plan plan, const void* in, int n_heads, void
 
 uly_status ulysses_seq_to_head_heads(uly_plan plan, const void* x_seq, int n_heads, void* x_head,
                                      void* stream) {
+  ULY_CALL_RANGE();
   return permute_heads(plan, x_seq, n_heads, x_head, true, stream);
 }
 
 uly_status ulysses_head_to_seq(uly_plan plan, const void* x_head, int n_heads, void* x_seq,
                                void* stream) {
+  ULY_CALL_RANGE();
   return permute_heads(plan, x_head, n_heads, x_seq, false, stream);
 }
 
 uly_status ulysses_attn_fwd(uly_plan plan, const void* q, const void* k, const void* v, void* o,
                             void* o_lo, float* lse, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = uly::attn_view(plan);
   if (p.S == 0) return ULY_OK;
@@ -377,6 +386,7 @@ uly_status ulysses_attn_fwd(uly_plan plan, const void* q, const void* k, const v
 uly_status ulysses_attn_bwd(uly_plan plan, const void* q, const void* k, const void* v,
                             const void* o, const void* o_lo, const float* lse, const void* d_o,
                             void* dq, void* dk, void* dv, void* workspace, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = uly::attn_view(plan);
   if (p.S == 0) return ULY_OK;
@@ -392,6 +402,7 @@ uly_status ulysses_attn_bwd(uly_plan plan, const void* q, const void* k, const v
 
 uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void* dq, const void* dk, const void* dv,
                                    int apply_rope, void* dqkv_seq, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   if (plan->p.rank >= 0) return reject_rank_plan(plan, "ulysses_head_to_seq_qkv");
   Plan& p = plan->p;
@@ -409,6 +420,7 @@ uly_status ulysses_head_to_seq_qkv(uly_plan plan, const void* dq, const void* dk
 
 uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void* x, const void* w, const void* dqkv,
                                 void* dx, float* dw, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
@@ -422,6 +434,7 @@ uly_status ulysses_qkv_proj_bwd(uly_plan plan, const void* x, const void* w, con
 
 uly_status ulysses_o_proj(uly_plan plan, const void* o_head, const void* wo, void* y,
                           void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
@@ -434,6 +447,7 @@ uly_status ulysses_o_proj(uly_plan plan, const void* o_head, const void* wo, voi
 
 uly_status ulysses_o_proj_bwd(uly_plan plan, const void* o_head, const void* wo, const void* dy,
                               void* do_head, float* dwo, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = uly::rows_view(plan);
   if (p.S == 0) return ULY_OK;
@@ -447,6 +461,7 @@ uly_status ulysses_o_proj_bwd(uly_plan plan, const void* o_head, const void* wo,
 }
 
 uly_status ulysses_sync_status(uly_plan plan, void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   cudaError_t e = cudaStreamSynchronize(as_stream(stream));
   if (e != cudaSuccess) return uly::cuda_fail(e, "stream synchronize");
@@ -464,6 +479,17 @@ uly_status ulysses_sync_status(uly_plan plan, void* stream) {
                                  "the range its scaled fp16 copy can hold");
     return fail((uly_status)st, "device reported status %d", st);
   }
+#ifdef ULY_DEBUG
+  const unsigned int n_perm = uly::debug_bounds_failures_permute(),
+                     n_fwd = uly::debug_bounds_failures_attn_fwd(),
+                     n_bwd = uly::debug_bounds_failures_attn_bwd(),
+                     n_gemm = uly::debug_bounds_failures_proj_gemm();
+  if (n_perm + n_fwd + n_bwd + n_gemm)
+    return fail(ULY_ERR_BOUNDS,
+                "debug build: global accesses outside their buffers were skipped (permute %u, "
+                "attn_fwd %u, attn_bwd %u, proj_gemm %u)",
+                n_perm, n_fwd, n_bwd, n_gemm);
+#endif
   uly::g_err[0] = 0;
   return ULY_OK;
 }
@@ -489,6 +515,7 @@ size_t ulysses_ring_workspace_bytes(uly_plan plan) {
 uly_status ulysses_ring_attn_fwd(uly_plan plan, const void* q_seq, const void* k_seq,
                                  const void* v_seq, void* o_seq, float* lse, void* workspace,
                                  void* stream) {
+  ULY_CALL_RANGE();
   if (!plan) return fail(ULY_ERR_INVALID_ARG, "plan is NULL");
   if (plan->p.rank >= 0) return reject_rank_plan(plan, "ulysses_ring_attn_fwd");
   Plan& p = plan->p;

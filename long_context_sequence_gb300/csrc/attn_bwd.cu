@@ -163,6 +163,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = rem - gg * a.nkb;                         // key block; 0 (most work) first
   const int nqi = (a.S - nb * BN + BMI - 1) / BMI;         // 64-row query tiles that see it
   const int n_items = a.group * nqi;
+  // element extents for the debug checks: row terms [P][hl][S], dQ [P][S][hl][D], dK/dV
+  // [P][S][gl][D]
+  const uint64_t n_ranks = gridDim.x / (uint64_t)per_rank;
+  const uint64_t ext_rows = n_ranks * a.hl * a.S, ext_q = n_ranks * a.S * a.hl * D,
+                 ext_kv = n_ranks * a.S * a.gl * D;
+  (void)ext_rows; (void)ext_q; (void)ext_kv;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -222,8 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qc = lane + 32 * e;
         const int qg = q0 + qc;
         const size_t idx = ((size_t)r * a.hl + hh) * a.S + qg;
-        rw[qc] = qg < a.S ? a.log2_scale - a.lse[idx] * 1.4426950408889634f : -INFINITY;
-        rw[64 + qc] = qg < a.S ? a.delta[idx] : 0.f;
+        const bool in = qg < a.S && ULY_IN_BOUNDS(idx, 1, ext_rows);
+        rw[qc] = in ? a.log2_scale - a.lse[idx] * 1.4426950408889634f : -INFINITY;
+        rw[64 + qc] = in ? a.delta[idx] : 0.f;
       }
       __syncwarp();
       if (lane == 0) {
@@ -472,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float x[4] = {__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
                         __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])};
           quad_transpose(x, lane);
-          if (full || q0 + 32 * w2 + 4 * c + b4 < a.S)
+          if ((full || q0 + 32 * w2 + 4 * c + b4 < a.S) &&
+              ULY_IN_BOUNDS(ptr + 4 * c * rs - a.dq_acc, 4, ext_q))
             red_add4(ptr + 4 * c * rs, x[0], x[1], x[2], x[3]);
         }
       }
@@ -494,7 +502,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
         uint32_t v[32];
         tmem_ld32(tbase + lane_off + 256 + which * D + 32 * c, v);
-        if (key_g < a.S) {
+        if (key_g < a.S &&
+            ULY_IN_BOUNDS(dst + 32 * c - (which ? a.dk : a.dv), 32, ext_kv)) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             auto sc = [&](int e) { return __uint_as_float(v[8 * j + e]) * m1 * m2; };
@@ -653,7 +662,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   const int64_t rowid = tid / TPR;       // row in [P][S][hl] order
   const int part = (int)(tid % TPR);
   float acc = 0.f;
-  if (rowid < rows) {
+  if (rowid < rows && ULY_IN_BOUNDS(rowid * D + part * 8, 8, (uint64_t)rows * D)) {
     const uint4 a = *reinterpret_cast<const uint4*>(o + rowid * D + part * 8);
     const uint4 b = *reinterpret_cast<const uint4*>(d_o + rowid * D + part * 8);
     uint4 c = make_uint4(0, 0, 0, 0);
@@ -682,7 +691,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
     const int64_t hh = rowid % hl;
     const int64_t rs = rowid / hl;     // r * S + s
     const int64_t r = rs / S, s = rs - r * S;
-    delta[(r * hl + hh) * S + s] = acc * exp2i(ex.w + ex.z);
+    if (ULY_IN_BOUNDS((r * hl + hh) * S + s, 1, rows))
+      delta[(r * hl + hh) * S + s] = acc * exp2i(ex.w + ex.z);
   }
 }
 
@@ -846,5 +856,7 @@ cudaError_t launch_attn_bwd(const Plan& p, const void* q, const void* k, const v
   if (p.D == 64) return launch_bwd_d<64>(p, q, k, v, o, o_lo, lse, d_o, dq, dk, dv, workspace, st);
   return launch_bwd_d<128>(p, q, k, v, o, o_lo, lse, d_o, dq, dk, dv, workspace, st);
 }
+
+ULY_DEBUG_COUNTER_READER(attn_bwd)
 
 }  // namespace uly

@@ -332,8 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // row offsets: output / accumulator [P][S][H][D], lse / state [P][H][S]
     auto srow = [&]() { return ((size_t)r * a.hl + hh) * a.S + row_g; };
     auto orow_off = [&]() { return (((size_t)r * a.S + row_g) * a.hl + hh) * D; };
+    // element extents of o (and acc) and of lse (and the running state), for the debug checks
+    // (a ring step launches the ranks ring_t .. P-1 only)
+    const uint64_t n_ranks = (kRing ? a.ring_t : 0) + gridDim.x / ((uint64_t)a.hl * a.n_mb);
+    const uint64_t ext_o = n_ranks * a.S * a.hl * D, ext_l = n_ranks * a.hl * a.S;
+    (void)ext_o; (void)ext_l;
     if (full_blk) {
-      const bool live = row_g < a.S;
+      const bool live = row_g < a.S && ULY_IN_BOUNDS(orow_off(), D, ext_o) &&
+                        ULY_IN_BOUNDS(srow(), 1, ext_l);
       // the state the rank's earlier steps left: O into TMEM before the first P V
       if (live) {
         m_used = a.mstate[srow()];
@@ -438,14 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(to + 32 * c, o);
-        if (live) {
+        if (live && ULY_IN_BOUNDS(orow_off() + 32 * c, 32, ext_o)) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             arow[8 * c + e] = make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
                                           __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
         }
       }
-      if (live) {
+      if (live && ULY_IN_BOUNDS(srow(), 1, ext_l)) {
         a.mstate[srow()] = m_used;
         a.lstate[srow()] = l;
       }
@@ -457,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(to + 32 * c, o);
-        if (row_g < a.S) {
+        if (row_g < a.S && ULY_IN_BOUNDS(orow_off() + 32 * c, 32, ext_o)) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             uint4 v;
@@ -482,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (row_g < a.S) a.lse[srow()] = (m_used + lg2_approx(l)) * 0.6931471805599453f;
+      if (row_g < a.S && ULY_IN_BOUNDS(srow(), 1, ext_l))
+        a.lse[srow()] = (m_used + lg2_approx(l)) * 0.6931471805599453f;
     }
   }
 
@@ -545,6 +552,7 @@ __global__ void __launch_bounds__(256) ring_pass_kernel(const uint4* __restrict_
     const int64_t r = i / shard8;
     const int64_t e = i - r * shard8;
     const int64_t d = (r + 1 == P ? 0 : r + 1) * shard8 + e;
+    if (!ULY_IN_BOUNDS(d, 1, total)) continue;
     k_dst[d] = __ldcs(k_src + i);
     v_dst[d] = __ldcs(v_src + i);
   }
@@ -641,5 +649,7 @@ cudaError_t launch_ring_attn(const Plan& p, const void* q_seq, const void* k_seq
   if (p.D == 64) return launch_ring_d<64>(p, q_seq, k_seq, v_seq, o_seq, lse, workspace, st);
   return launch_ring_d<128>(p, q_seq, k_seq, v_seq, o_seq, lse, workspace, st);
 }
+
+ULY_DEBUG_COUNTER_READER(attn_fwd)
 
 }  // namespace uly

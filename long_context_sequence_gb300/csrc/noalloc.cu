@@ -59,6 +59,7 @@ extern "C" uly_status ulysses_attn_bwd_noalloc(uly_plan plan, const void* q, con
                                                const void* v, const void* o, const void* o_lo,
                                                const float* lse, const void* d_o, void* dq,
                                                void* dk, void* dv, void* stream) {
+  ULY_CALL_RANGE();
   using namespace uly;
   if (!plan) return set_error(ULY_ERR_INVALID_ARG, "plan is NULL");
   const Plan& p = attn_view(plan);

@@ -120,6 +120,9 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
   const int hq = H / P, hk = G / P;
   const int64_t n_blocks = (S + kThreads / upr - 1) / (kThreads / upr);
   const size_t esz = kFp32In ? 4 : 2;
+  const uint64_t ext_in = (uint64_t)S * C * D, ext_q = (uint64_t)P * S * hq * D,
+                 ext_kv = (uint64_t)P * S * hk * D;   // element extents (debug checks)
+  (void)ext_in; (void)ext_q; (void)ext_kv;
   for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
     const TokenChunk tc = token_chunk(b, upr, S);
     if (!tc.valid) continue;
@@ -132,16 +135,30 @@ __global__ void __launch_bounds__(kThreads) seq_to_head_kernel(
     for (int c = 0; c < C; ++c) {
       const char* src = row + (size_t)c * D * esz;
       __nv_bfloat16* dst;
+      size_t doff;
+      uint64_t dext;
       if (c < H) {
         const int r2 = c / hq, hh = c - r2 * hq;
-        dst = q + (((size_t)r2 * S + s) * hq + hh) * D;
+        doff = (((size_t)r2 * S + s) * hq + hh) * D;
+        dst = q + doff;
+        dext = ext_q;
       } else if (c < H + G) {
         const int g = c - H, r2 = g / hk, hh = g - r2 * hk;
-        dst = k + (((size_t)r2 * S + s) * hk + hh) * D;
+        doff = (((size_t)r2 * S + s) * hk + hh) * D;
+        dst = k + doff;
+        dext = ext_kv;
       } else {
         const int g = c - H - G, r2 = g / hk, hh = g - r2 * hk;
-        dst = v + (((size_t)r2 * S + s) * hk + hh) * D;
+        doff = (((size_t)r2 * S + s) * hk + hh) * D;
+        dst = v + doff;
+        dext = ext_kv;
       }
+      (void)doff; (void)dext;
+      const size_t soff = ((size_t)s * C + c) * D;
+      (void)soff;
+      if (!ULY_IN_BOUNDS(soff + e_lo, 8, ext_in) || !ULY_IN_BOUNDS(soff + e_hi, 8, ext_in) ||
+          !ULY_IN_BOUNDS(doff + e_lo, 8, dext) || !ULY_IN_BOUNDS(doff + e_hi, 8, dext))
+        continue;
       float lo[8], hi[8];
       uint4 raw_lo, raw_hi;
       load8<kFp32In>(src, e_lo, lo, raw_lo);
@@ -178,6 +195,9 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
   const int upr = D / 16;
   const int hq = H / P, hk = G / P;
   const int64_t n_blocks = (S + kThreads / upr - 1) / (kThreads / upr);
+  const uint64_t ext_out = (uint64_t)S * C * D, ext_q = (uint64_t)P * S * hq * D,
+                 ext_kv = (uint64_t)P * S * hk * D;   // element extents (debug checks)
+  (void)ext_out; (void)ext_q; (void)ext_kv;
   for (int64_t b = blockIdx.x; b < n_blocks; b += gridDim.x) {
     const TokenChunk tc = token_chunk(b, upr, S);
     if (!tc.valid) continue;
@@ -189,17 +209,31 @@ __global__ void __launch_bounds__(kThreads) head_to_seq_qkv_kernel(
 #pragma unroll 2
     for (int c = 0; c < C; ++c) {
       const __nv_bfloat16* src;
+      size_t soff;
+      uint64_t sext;
       if (c < H) {
         const int r2 = c / hq, hh = c - r2 * hq;
-        src = dq + (((size_t)r2 * S + s) * hq + hh) * D;
+        soff = (((size_t)r2 * S + s) * hq + hh) * D;
+        src = dq + soff;
+        sext = ext_q;
       } else if (c < H + G) {
         const int g = c - H, r2 = g / hk, hh = g - r2 * hk;
-        src = dk + (((size_t)r2 * S + s) * hk + hh) * D;
+        soff = (((size_t)r2 * S + s) * hk + hh) * D;
+        src = dk + soff;
+        sext = ext_kv;
       } else {
         const int g = c - H - G, r2 = g / hk, hh = g - r2 * hk;
-        src = dv + (((size_t)r2 * S + s) * hk + hh) * D;
+        soff = (((size_t)r2 * S + s) * hk + hh) * D;
+        src = dv + soff;
+        sext = ext_kv;
       }
+      (void)soff; (void)sext;
       __nv_bfloat16* dst = row + (size_t)c * D;
+      const size_t doff = ((size_t)s * C + c) * D;
+      (void)doff;
+      if (!ULY_IN_BOUNDS(soff + e_lo, 8, sext) || !ULY_IN_BOUNDS(soff + e_hi, 8, sext) ||
+          !ULY_IN_BOUNDS(doff + e_lo, 8, ext_out) || !ULY_IN_BOUNDS(doff + e_hi, 8, ext_out))
+        continue;
       const uint4 raw_lo = ld_stream(src + e_lo), raw_hi = ld_stream(src + e_hi);
       if (kRope && c < H + G) {
         float lo[8], hi[8];
@@ -244,6 +278,9 @@ __global__ void __launch_bounds__(kThreads) permute_heads_kernel(
       const int r2 = h / hl, hh = h - r2 * hl;
       const size_t seq_off = ((size_t)s * n + h) * D + e;
       const size_t head_off = (((size_t)r2 * S + s) * hl + hh) * D + e;
+      if (!ULY_IN_BOUNDS(seq_off, 8, (uint64_t)S * n * D) ||
+          !ULY_IN_BOUNDS(head_off, 8, (uint64_t)S * n * D))
+        continue;
       if (kToHead)
         st_stream(out + head_off, ld_stream(in + seq_off));
       else
@@ -313,5 +350,7 @@ cudaError_t launch_permute_heads(const Plan& p, const void* in, int n_heads, voi
     permute_heads_kernel<false><<<grid, kThreads, 0, st>>>(i, o, p.S, p.P, n_heads, p.D);
   return cudaGetLastError();
 }
+
+ULY_DEBUG_COUNTER_READER(permute)
 
 }  // namespace uly

@@ -176,9 +176,14 @@ __global__ void __launch_bounds__(128, 1)
           float* ocol = static_cast<float*>(out) + gm;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (gn + j < N) ocol[(size_t)(gn + j) * M] = __uint_as_float(r[j]);
+            if (gn + j < N && ULY_IN_BOUNDS((size_t)(gn + j) * M + gm, 1, (uint64_t)M * N))
+              ocol[(size_t)(gn + j) * M] = __uint_as_float(r[j]);
         }
-      } else if (gm < M && gn < N) {
+      } else if (gm < M && gn < N &&
+                 ULY_IN_BOUNDS(
+                     (out_split ? ((size_t)(gn / out_split) * M + gm) * out_split + (gn % out_split)
+                                : (size_t)gm * N + gn),
+                     gn + 32 <= N ? 32 : N - gn, (uint64_t)M * N)) {
         // row-major [M][N], or the head layout [N/split][M][split] (32-column chunks never
         // straddle two parts since split is a multiple of 64)
         const size_t row_off = out_split ? ((size_t)(gn / out_split) * M + gm) * out_split +
@@ -315,5 +320,7 @@ cudaError_t launch_o_proj_bwd(const Plan& p, const void* o_head, const void* wo,
   }
   return cudaSuccess;
 }
+
+ULY_DEBUG_COUNTER_READER(proj_gemm)
 
 }  // namespace uly

@@ -11,7 +11,38 @@ namespace uly {
 
 // Status codes shared with the C ABI (ulysses.h).
 enum : int { kOk = 0, kErrInvalid = 1, kErrUnsupported = 2, kErrCuda = 3, kErrOom = 4,
-             kErrTimeout = 5, kErrRange = 6 };
+             kErrTimeout = 5, kErrRange = 6, kErrBounds = 7 };
+
+// ---------------------------------------------------------------- debug build checks
+// Built with -DULY_DEBUG (libulysses_debug.so), every global index a kernel computes is
+// checked against its buffer's extent as the kernel's own size arguments give it.  An index
+// outside counts in this translation unit's failure counter and the access is skipped;
+// ulysses_sync_status reports the count as ULY_ERR_BOUNDS.  The release build compiles the
+// checks to `true` and has no counter.
+#ifdef ULY_DEBUG
+static __device__ unsigned int g_uly_bounds_failures;
+__device__ __forceinline__ bool in_bounds(uint64_t first, uint64_t count, uint64_t extent) {
+  if (first + count <= extent) return true;
+  atomicAdd(&g_uly_bounds_failures, 1u);
+  return false;
+}
+// Host side: the counter of the translation unit that expands it (read, then cleared).
+#define ULY_DEBUG_COUNTER_READER(name)                                                  \
+  unsigned int debug_bounds_failures_##name() {                                        \
+    unsigned int n = 0, z = 0;                                                          \
+    if (cudaMemcpyFromSymbol(&n, g_uly_bounds_failures, sizeof(n)) != cudaSuccess) {   \
+      cudaGetLastError();                                                               \
+      return 0;                                                                         \
+    }                                                                                   \
+    if (n) cudaMemcpyToSymbol(g_uly_bounds_failures, &z, sizeof(z));                    \
+    return n;                                                                           \
+  }
+#define ULY_IN_BOUNDS(first, count, extent) \
+  ::uly::in_bounds((uint64_t)(first), (uint64_t)(count), (uint64_t)(extent))
+#else
+#define ULY_DEBUG_COUNTER_READER(name)
+#define ULY_IN_BOUNDS(first, count, extent) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -166,6 +166,7 @@ uly_status ulysses_a2a_table(const uly_config* cfg, int32_t rank, int32_t to_hea
 uly_status ulysses_a2a_pack_qkv(uly_plan plan, const void* qkv_local, int in_fp32,
                                 int apply_rope, void* send_q, void* send_k, void* send_v,
                                 void* stream) {
+  ULY_CALL_RANGE();
   uly_status s = uly::need_rank_plan(plan, "ulysses_a2a_pack_qkv");
   if (s != ULY_OK) return s;
   const Plan& v = plan->shard;
@@ -209,17 +210,20 @@ static uly_status pack_or_unpack(uly_plan plan, const void* in, int n_heads, voi
 
 uly_status ulysses_a2a_pack_heads(uly_plan plan, const void* x_local, int n_heads, void* send,
                                   void* stream) {
+  ULY_CALL_RANGE();
   return pack_or_unpack(plan, x_local, n_heads, send, true, stream);
 }
 
 uly_status ulysses_a2a_unpack_heads(uly_plan plan, const void* recv, int n_heads,
                                     void* x_local, void* stream) {
+  ULY_CALL_RANGE();
   return pack_or_unpack(plan, recv, n_heads, x_local, false, stream);
 }
 
 uly_status ulysses_a2a_unpack_qkv(uly_plan plan, const void* recv_dq, const void* recv_dk,
                                   const void* recv_dv, int apply_rope, void* dqkv_local,
                                   void* stream) {
+  ULY_CALL_RANGE();
   uly_status s = uly::need_rank_plan(plan, "ulysses_a2a_unpack_qkv");
   if (s != ULY_OK) return s;
   const Plan& v = plan->shard;
@@ -242,6 +246,7 @@ uly_status ulysses_a2a_unpack_qkv(uly_plan plan, const void* recv_dq, const void
 uly_status ulysses_a2a_exchange(uly_plan plan, void* comm, int32_t n_buffers,
                                 const void* const* send, void* const* recv,
                                 const uint64_t* bytes_per_peer, void* stream) {
+  ULY_CALL_RANGE();
   uly_status s = uly::need_rank_plan(plan, "ulysses_a2a_exchange");
   if (s != ULY_OK) return s;
   if (!comm || !send || !recv || !bytes_per_peer)
@@ -306,6 +311,7 @@ uly_status ulysses_nccl_unique_id(uint8_t id[128]) {
 
 uly_status ulysses_nccl_comm_init(int32_t nranks, int32_t rank, const uint8_t id[128],
                                   void** comm) {
+  ULY_CALL_RANGE();
   if (!id || !comm) return uly::set_error(ULY_ERR_INVALID_ARG, "NULL argument");
   *comm = nullptr;
   if (nranks < 1 || rank < 0 || rank >= nranks)

@@ -6,9 +6,22 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/ulysses.h"
 
 namespace uly {
+
+// An NVTX range over one C-ABI call, named after the call: the calls show up as ranges in
+// the Nsight tools, and ncu can select a call's kernels (--nvtx --nvtx-include "name/").
+// Without a tool attached a range costs a few nanoseconds.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+#define ULY_CALL_RANGE() ::uly::CallRange uly_call_range_(__func__)
 
 // RoPE angles are kept as a two-level table so that positions up to 2^20 and beyond
 // need little memory: for s = sh * kRopeL + sl, (cos, sin)(s * w_i) is rebuilt from
@@ -100,6 +113,14 @@ bool make_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t dims[4],
                        const char** err);
 
 int num_sms(int device);
+
+#ifdef ULY_DEBUG
+// Debug build: the out-of-bounds counters of the kernel files (read and cleared).
+unsigned int debug_bounds_failures_permute();
+unsigned int debug_bounds_failures_attn_fwd();
+unsigned int debug_bounds_failures_attn_bwd();
+unsigned int debug_bounds_failures_proj_gemm();
+#endif
 
 // Copies p's shared state into a view of other sizes (same device, tables, status word).
 void make_view(const Plan& src, Plan& dst, int64_t S, int P, int H, int G);
