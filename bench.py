@@ -45,15 +45,17 @@ def attn_flops(S, H, D):
     return fwd, 2.5 * fwd
 
 
-# DRAM bytes of one ulysses_attn_bwd call at the bench workload (S=131072), summed over its
-# kernels (bwd_pre, 2 x to_f16, attn_bwd_kernel, bwd_dq), from one ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none).
-# Valid only for the kernel source it was taken on: the figure is dropped (null) as soon as
-# the hash of that source changes.
-BWD_TRAFFIC = {"bytes": (4.30 + 4.26 + (0.26847 + 0.21473) + (0.26849 + 0.21394) + 17.60 + 8.94
-                         + 2.15 + 1.04) * 1e9,
+# DRAM bytes of one ulysses_attn_bwd call at the bench workload (S=131072), summed over its six
+# kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none):
+# attn_bwd_kernel from one capture of that kernel alone, one launch, at S=131072 (17.22 GB read,
+# 8.71 GB written); the five streaming kernels (largest magnitudes, pre-pass, two fp16 copies, dQ
+# conversion), whose bytes are a fixed number per element, from a capture of one call at S=32768
+# scaled by 4.  Valid only for the kernel source it was taken on: the figure is dropped (null) as
+# soon as the hash of that source changes.
+BWD_TRAFFIC = {"bytes": (17.22 + 8.71) * 1e9 + 4 * (0.674322 + 2.100248 + 0.081305 + 0.081330
+                                                    + 0.763634) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "491f8e69edc769288d18475f1c606720dbecc88e1b462a9bd5c97b62209f99fc"}
+               "source_sha256": "b6d68dc6ec1c47132aee55c9a288e0997cfcda66e9ef7ab95537ae216f505b7c"}
 
 
 def bwd_traffic(seq_len):
