@@ -36,7 +36,8 @@ def _check_fwd_rows(q, k, v, o, lse, rows, P, H, G, tag):
         ro, rl = O.causal_attention_rows(synthetic.bf16_to_f64(q[r]), synthetic.bf16_to_f64(k[r]),
                                          synthetic.bf16_to_f64(v[r]), rows)
         assert_close(o_h[r][rows], ro, "%s o[rank %d]" % (tag, r))
-        assert_close_f32(lse_h[r][:, rows], rl, "%s lse[rank %d]" % (tag, r))
+        e = assert_close_f32(lse_h[r][:, rows], rl, "%s lse[rank %d]" % (tag, r))
+        print("%s lse[rank %d] max|err| %.3g (max|lse| %.3g)" % (tag, r, e, np.abs(rl).max()))
 
 
 @pytest.mark.parametrize("S", [32768, 131072])
@@ -54,10 +55,12 @@ def test_forward_8b_block_sampled_rows(S):
     _check_fwd_rows(q, k, v, o, lse, rows, P, H8B, G8B, "S=%d" % S)
 
 
-def _bwd_check(S, P, H, G, D, std, n_rows, tail, tag):
+def _bwd_check(S, P, H, G, D, std, n_rows, tail, tag, sigma_do=1.0):
+    """sigma_do: std of the upstream gradient; errors are compared divided by it (the
+    2e-2 / 2e-3 bounds are then scale-invariant)."""
     plan = U.ulysses_plan(U.make_config(S, P, 64, H, G, D))
     q, k, v = _gen(S, P, H, G, D, std)
-    do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D))
+    do = synthetic.normal_bf16(synthetic.SEED_DO, 0, (P, S, H // P, D), std=sigma_do)
     qg, kg, vg, dog = (dev_bf16(a) for a in (q, k, v, do))
     o, o_lo = empty_bf16((P, S, H // P, D)), empty_bf16((P, S, H // P, D))
     lse = torch.empty((P, H // P, S), dtype=torch.float32, device="cuda")
@@ -72,9 +75,10 @@ def _bwd_check(S, P, H, G, D, std, n_rows, tail, tag):
     for r in ranks:
         qf, kf, vf, dof = (synthetic.bf16_to_f64(a[r]) for a in (q, k, v, do))
         rdq, rdk, rdv = O.causal_attention_bwd_rows(qf, kf, vf, dof, rows, S - tail)
-        assert_close(dq_h[r][rows], rdq, "%s dq[rank %d] sampled rows" % (tag, r))
-        assert_close(dk_h[r][S - tail:], rdk, "%s dk[rank %d] tail keys" % (tag, r))
-        assert_close(dv_h[r][S - tail:], rdv, "%s dv[rank %d] tail keys" % (tag, r))
+        sg = sigma_do
+        assert_close(dq_h[r][rows] / sg, rdq / sg, "%s dq[rank %d] sampled rows" % (tag, r))
+        assert_close(dk_h[r][S - tail:] / sg, rdk / sg, "%s dk[rank %d] tail keys" % (tag, r))
+        assert_close(dv_h[r][S - tail:] / sg, rdv / sg, "%s dv[rank %d] tail keys" % (tag, r))
     return plan
 
 
@@ -102,6 +106,13 @@ def test_backward_8b_block_128k_sampled_rows():
     """The benchmarked workload itself, S=131072, P=8: dQ on sampled rows, dK/dV on the last
     256 keys, three ranks checked."""
     _bwd_check(131072, 8, H8B, G8B, D8B, STD8B, 128, 256, "S=128K")
+
+
+def test_backward_8b_block_128k_training_step_gradients():
+    """The benchmarked workload with the upstream gradient of a token-averaged loss,
+    dO ~ N(0, 1e-6^2): the per-call power-of-two scaling keeps fp16's precision; errors
+    divided by sigma_dO meet the same bounds as the dO ~ N(0, 1) case."""
+    _bwd_check(131072, 8, H8B, G8B, D8B, STD8B, 128, 256, "S=128K dO~1e-6", sigma_do=1e-6)
 
 
 def test_million_token_head_group_fwd_bwd():
