@@ -152,7 +152,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "scaling": "strong", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w["name"], "seq_len": S, "P": w["P"], "hidden": w["hidden"],
                        "n_q_heads": w["H"], "n_kv_heads": w["G"], "head_dim": w["D"]},
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
