@@ -96,9 +96,12 @@ typedef struct uly_config {
 typedef struct uly_plan_s *uly_plan;
 
 /* Validate cfg and build a plan: copies cfg, builds the RoPE angle tables (fp64 on the
- * host, stored fp32 on the device) and a device status word.  No kernel is launched.
- * Returns ULY_ERR_INVALID_ARG / ULY_ERR_UNSUPPORTED for bad configs, ULY_ERR_OOM or
- * ULY_ERR_CUDA if its buffers cannot be made.  The current CUDA device is the plan's. */
+ * host, stored fp32 on the device) and a device status word, and looks up the device address
+ * of the library's fixed backward scratch (ulysses_attn_bwd_noalloc); with the runtime's
+ * default lazy module loading, the first plan on a device is what loads that 64 MiB array
+ * there.  No kernel is launched.  Returns ULY_ERR_INVALID_ARG / ULY_ERR_UNSUPPORTED for bad
+ * configs, ULY_ERR_OOM or ULY_ERR_CUDA if its buffers cannot be made.  The current CUDA
+ * device is the plan's.  A plan does not survive a reset of its device. */
 uly_status ulysses_plan(const uly_config *cfg, uly_plan *out);
 
 /* Frees the plan's buffers.  NULL is allowed.  Synchronises the device first. */
