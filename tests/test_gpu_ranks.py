@@ -242,3 +242,28 @@ def test_nccl_exchange_in_a_one_rank_group(block):
         assert ei.value.status == U.ULY_ERR_INVALID_ARG and "communicator" in str(ei.value)
     finally:
         U.ulysses_nccl_comm_destroy(comm)
+
+
+@pytest.mark.parametrize("theta", [0.0, THETA])
+def test_rank_pack_of_fp32_projection_output(theta):
+    """An fp32 projection output packed by a rank plan (rounded to bf16 on the way, RoPE at
+    the shard's global positions when theta > 0) equals the virtual path's seq->head of the
+    same fp32 tensor, block for block, bit for bit."""
+    cfg = U.make_config(S, P, HID, H, G, D, rope_theta=theta)
+    virt = U.ulysses_plan(cfg)
+    sh = virt.shapes()
+    x = synthetic.normal_f64(0, synthetic.TENSOR_QKV, (S, H + 2 * G, D), std=1.28).astype(np.float32)
+    xg = torch.from_numpy(x).cuda()
+    q, k, v = empty_bf16(sh["q"]), empty_bf16(sh["k"]), empty_bf16(sh["v"])
+    U.ulysses_seq_to_head(virt, xg, q, k, v, apply_rope=theta > 0)
+    for r in range(P):
+        pl = U.ulysses_plan_rank(cfg, r)
+        rs = pl.shapes()
+        sq, sk, sv = empty_bf16(rs["q"]), empty_bf16(rs["k"]), empty_bf16(rs["v"])
+        U.ulysses_a2a_pack_qkv(pl, xg[r * N:(r + 1) * N].contiguous(), sq, sk, sv,
+                               apply_rope=theta > 0)
+        assert U.ulysses_sync_status(pl) == U.ULY_OK, U.ulysses_last_error()
+        for p in range(P):
+            assert torch.equal(sq[p], q[p, r * N:(r + 1) * N])
+            assert torch.equal(sk[p], k[p, r * N:(r + 1) * N])
+            assert torch.equal(sv[p], v[p, r * N:(r + 1) * N])
