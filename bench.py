@@ -55,7 +55,7 @@ def attn_flops(S, H, D):
 BWD_TRAFFIC = {"bytes": (17.22 + 8.71) * 1e9 + 4 * (0.674322 + 2.100248 + 0.081305 + 0.081330
                                                     + 0.763634) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "b6d68dc6ec1c47132aee55c9a288e0997cfcda66e9ef7ab95537ae216f505b7c"}
+               "source_sha256": "7d7f402dcddf7a10366fa080770571909dd638a31fc3d586cae2948264545667"}
 
 
 def bwd_traffic(seq_len):

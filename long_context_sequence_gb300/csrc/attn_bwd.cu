@@ -41,10 +41,10 @@
 // Then |dP' - D'| <= 2 D max|dO'| max|v'| and dS' = P' (dP' - D') stays below 2^15: no fp16
 // operand can overflow, and for ordinary data none is subnormal.  The outputs take the
 // inverse powers exactly (power-of-two factors in the epilogues): dV = acc / (scale
-// 2^(kp+edo)), dK = 2^-(kp+edo+ev+eq) acc, dQ = 2^-(kp+edo+ev-eq) acc.  Scaling any input by a power of
-// two therefore leaves every fp16 operand bit for bit as it was and scales the outputs
-// exactly.  A tensor whose largest magnitude lies beyond the exponents' range (|e| <= 60)
-// would saturate: the call reports ULY_ERR_RANGE through the status word.
+// 2^(kp+edo)), dK = 2^-(kp+edo+ev+eq) acc, dQ = 2^-(kp+edo+ev-eq) acc.  Scaling any input by
+// a power of two therefore leaves every fp16 operand bit for bit as it was and scales the
+// outputs exactly.  A tensor whose largest magnitude lies beyond the exponents' range
+// (|e| <= 60) would saturate: the call reports ULY_ERR_RANGE through the status word.
 // TMEM (512 columns): region X at [128X, 128X+128): S^T [0,64) -> dQ^T; dP^T [64,128) ->
 // P^T of warpgroup w2 at [64+32 w2, 64+32 w2+16).  dV [256,256+D), dK [256+D, 256+2D).
 #include <cmath>
@@ -186,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(drain_acc, 1);
     *abort_flag = 0;
-
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
