@@ -40,6 +40,19 @@ METRIC = "causal attn fwd+bwd TFLOPS at S=128K (whole step incl. projection and 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def workload_config(S, P, parallelism):
+    """The workload a line measures (the same dict for both arms at one N)."""
+    w = WORKLOAD
+    return {"workload": w["name"], "seq_len": S, "P": P, "hidden": w["hidden"],
+            "n_q_heads": w["H"], "n_kv_heads": w["G"], "head_dim": w["D"],
+            "rope_theta": w["theta"], "global_batch": 1, "parallelism": parallelism,
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+def parallelism_of(world, P):
+    return "ulysses-sp%d" % P if world > 1 else "single GPU, P=%d virtual ranks" % P
+
+
 def attn_flops(S, H, D):
     fwd = 2.0 * S * S * D * H          # causal: half of the dense 4 S^2 D H
     return fwd, 2.5 * fwd
@@ -153,8 +166,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
             "scaling": "strong", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w["name"], "seq_len": S, "P": w["P"], "hidden": w["hidden"],
-                       "n_q_heads": w["H"], "n_kv_heads": w["G"], "head_dim": w["D"]},
+            "config": workload_config(S, w["P"] if args.gpus <= 1 else args.gpus,
+                                      parallelism_of(args.gpus, w["P"] if args.gpus <= 1 else args.gpus)),
             "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -359,10 +372,7 @@ def run_sharded(args, U, world, rank, local, dev, dist):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (device torch.randn, seeded; X~N(0,1), W~N(0,0.02^2), dO~N(0,1))",
-            "config": {"workload": w["name"], "seq_len": S, "P": P, "hidden": hidden,
-                       "n_q_heads": H, "n_kv_heads": G, "head_dim": D, "rope_theta": theta,
-                       "global_batch": 1, "parallelism": "ulysses-sp%d" % P,
-                       "l2": "inputs larger than L2 (no flush)"},
+            "config": workload_config(S, P, "ulysses-sp%d" % P),
             "roofline": {"kernel": "ulysses_attn_bwd", "bound": "tensor", "achieved": bwd_tf,
                          "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                          "frac": bwd_tf / peaks["bf16_tflops_sustained"], "traffic": None,
@@ -705,10 +715,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (device torch.randn, seeded; X~N(0,1), W~N(0,0.02^2), dO~N(0,1))",
-            "config": {"workload": w["name"], "seq_len": S, "P": P, "hidden": hidden,
-                       "n_q_heads": H, "n_kv_heads": G, "head_dim": D, "rope_theta": theta,
-                       "global_batch": 1, "parallelism": "single GPU, P=%d virtual ranks" % P,
-                       "l2": "inputs larger than L2 (no flush)"},
+            "config": workload_config(S, P, parallelism_of(world, P)),
             "roofline": dict({"kernel": "ulysses_attn_bwd", "bound": "tensor",
                               "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
                               "frac": bwd_tflops / peak, "traffic": bwd_traffic(S),
