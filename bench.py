@@ -60,15 +60,15 @@ def attn_flops(S, H, D):
 
 # DRAM bytes of one ulysses_attn_bwd call at the bench workload (S=131072), summed over its six
 # kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none):
-# attn_bwd_kernel from one capture of that kernel alone, one launch, at S=131072 (17.22 GB read,
-# 8.71 GB written); the five streaming kernels (largest magnitudes, pre-pass, two fp16 copies, dQ
+# attn_bwd_kernel from one capture of that kernel alone, one launch, at S=131072 (17.35 GB read,
+# 8.76 GB written); the five streaming kernels (largest magnitudes, pre-pass, two fp16 copies, dQ
 # conversion), whose bytes are a fixed number per element, from a capture of one call at S=32768
 # scaled by 4.  Valid only for the kernel source it was taken on: the figure is dropped (null) as
 # soon as the hash of that source changes.
-BWD_TRAFFIC = {"bytes": (17.22 + 8.71) * 1e9 + 4 * (0.674322 + 2.100248 + 0.081305 + 0.081330
+BWD_TRAFFIC = {"bytes": (17.354 + 8.760) * 1e9 + 4 * (0.674322 + 2.100248 + 0.081305 + 0.081330
                                                     + 0.763634) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "7d7f402dcddf7a10366fa080770571909dd638a31fc3d586cae2948264545667"}
+               "source_sha256": "aff5a606f9fc75af79991a8aab62ae61b5c0fbde0406dea1e321d6c85229e179"}
 
 
 def bwd_traffic(seq_len):

@@ -14,10 +14,13 @@
 //   bwd_main  one CTA per (rank, KV head, 128-key block).  Work items are (64-row query
 //             tile, query head of the group) pairs from the diagonal on.  Items alternate
 //             between two TMEM regions so that one item's tensor work overlaps the other's
-//             element-wise work.  Two threads issue the MMAs (one thread issues a
-//             tcgen05.mma about every 58 cycles whatever its size, and these are small):
-//             issuer A S^T and dQ^T of both regions, issuer B dP^T and every dV and dK
-//             (the accumulators both regions share, so one thread orders them):
+//             element-wise work.  Two threads issue the MMAs: issuer A S^T and dQ^T of both
+//             regions, issuer B dP^T and every dV and dK (the accumulators both regions
+//             share, so one thread orders them).  A thread issuing a tcgen05.mma stalls
+//             while the tensor pipe's queue is full, and it serves its barriers in program
+//             order, so one issuer would leave a region's ready MMAs behind the other
+//             region's.  The pipe runs MMAs in issue order; issuer B holds dV/dK(it) until
+//             A has issued dQ^T(it), which the region's next S^T waits for:
 //               MMA1   S^T = K Q^T, dP^T = V dO^T            (M = 128 keys, N = 64 rows)
 //               8 warps per region, thread = key row, warpgroup = 32 query columns:
 //                      P^T = scale*exp(S^T scale - lse) -> TMEM (fp16, over dP^T),
@@ -154,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s_full + 13);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
   volatile int* decision = abort_flag + 1;   // [2 regions][2]: group-wait outcomes
+  volatile int* dq_issued = decision + 4;    // items whose dQ^T issuer A has issued
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int per_rank = a.gl * a.nkb;
@@ -186,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(drain_acc, 1);
     *abort_flag = 0;
+    *dq_issued = 0;
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -288,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tbase + 128 * X, dK_mn + ((kk * 2048) >> 4), dDS_mn + ((kk * 2048) >> 4), id_q,
                  kk > 0 ? 1u : 0u);
         mma_commit(&dq_full[X]);
+        *dq_issued = it + 1;
         return true;
       };
       // Pairs, one item per region: dQ^T of both, then S^T of the next two.  (Serving
@@ -331,6 +337,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; alive && it < n_items; ++it) {
         const int X = it & 1, st = it % NST;
         if (!mbar_wait(&p_full[X], (it >> 1) & 1, wc)) { alive = false; break; }
+        // Let dQ^T(it), which a region's next S^T waits for, enter the tensor pipe ahead of
+        // dV/dK(it) (the pipe runs MMAs in issue order).  Only an ordering preference: the
+        // wait is bounded and gives up if the CTA aborts.
+        for (uint32_t n = 0; *dq_issued <= it && n < (1u << 22) && !*wc.abort; ++n) {
+        }
         tc_fence_after();
         const uint64_t dQ_mn = sdesc_sw128(smem_u32(smem + L::kQ + st * L::kItem), kBox64, 1024);
         const uint64_t dDO_mn = sdesc_sw128(smem_u32(smem + L::kDO + st * L::kItem), kBox64, 1024);
