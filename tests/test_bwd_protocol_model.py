@@ -3,7 +3,8 @@
 The backward kernel's roles are re-stated here as a model:
 - the TMA producer: K and V once, then each item's Q, dO and row terms through a 4-stage ring;
 - issuer A: S^T and dQ^T, in region pairs;
-- issuer B: dP^T, dV and dK, in item order;
+- issuer B: dP^T, dV and dK, in item order, each item's dV/dK only after issuer A has issued
+  that item's dQ^T (a shared counter, an ordering preference the kernel bounds);
 - two element-wise groups, one per TMEM region, items alternating between the regions.
 
 The model uses the same mbarriers, arrival counts, parities and wait orders as the kernel. The
@@ -50,6 +51,7 @@ class Model:
         self.ew1, self.ew2 = set(), set()   # items whose element-wise passes are done
         self.copies = []
         self.queue = {"A": [], "B": []}
+        self.dq_issued = 0               # items whose dQ^T issuer A has queued
 
     def done(self, op, it):
         return (op, it) in self.executed
@@ -119,6 +121,7 @@ class Model:
                 yield
             q.append(("DQ", it))
             q.append(("commit", self.dq_full[X]))
+            self.dq_issued = it + 1
 
         for it in range(min(2, self.n)):
             yield from mma_s(it)
@@ -148,6 +151,8 @@ class Model:
         for it in range(self.n):
             X, st = it & 1, it % NST
             while not self.p_full[X].done(it >> 1):
+                yield
+            while self.dq_issued <= it:
                 yield
             q.append(("DV", it))
             q.append(("DK", it))
