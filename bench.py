@@ -60,15 +60,15 @@ def attn_flops(S, H, D):
 
 # DRAM bytes of one ulysses_attn_bwd call at the bench workload (S=131072), summed over its six
 # kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none):
-# attn_bwd_kernel from one capture of that kernel alone, one launch, at S=131072 (17.35 GB read,
-# 8.76 GB written); the five streaming kernels (largest magnitudes, pre-pass, two fp16 copies, dQ
+# attn_bwd_kernel from one capture of that kernel alone, one launch, at S=131072 (17.57 GB read,
+# 8.84 GB written); the five streaming kernels (largest magnitudes, pre-pass, two fp16 copies, dQ
 # conversion), whose bytes are a fixed number per element, from a capture of one call at S=32768
 # scaled by 4.  Valid only for the kernel source it was taken on: the figure is dropped (null) as
 # soon as the hash of that source changes.
-BWD_TRAFFIC = {"bytes": (17.354 + 8.760) * 1e9 + 4 * (0.674322 + 2.100248 + 0.081305 + 0.081330
-                                                    + 0.763634) * 1e9,
+BWD_TRAFFIC = {"bytes": (17.569 + 8.838) * 1e9 + 4 * (0.673954 + 2.102759 + 0.081413 + 0.081357
+                                                    + 0.771625) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "aff5a606f9fc75af79991a8aab62ae61b5c0fbde0406dea1e321d6c85229e179"}
+               "source_sha256": "583496fad9ec3543f5ec8a0811eae26a783e8f38fab0fc47a47d17eb9f82fe77"}
 
 
 def bwd_traffic(seq_len):

@@ -27,8 +27,10 @@
 //                      dS = P (dP - D) -> smem (fp16, 128-byte swizzle)
 //               MMA2   dQ^T = K^T dS^T (M = d, over S^T), dV += P^T dO, dK += dS^T Q
 //               the same warps, thread = d: dQ^T -> fp32 reductions into the workspace
-//                      accumulator (one 128-byte run per warp and row);
-//   bwd_dq    fp32 dQ accumulator -> bf16.
+//                      accumulator, which keeps four query rows of one (head, d) together
+//                      ([P][S4/4][hl][D][4]): a thread adds its own four rows in one
+//                      16-byte reduction, a warp 512 contiguous bytes;
+//   bwd_dq    fp32 dQ accumulator -> bf16 [P][S][hl][D].
 // Every MMA runs on fp16 operands, and P, dS keep 11 significand bits, which the long
 // dK/dQ sums need.  fp16 holds full precision only in [2^-14, 65504], while the bf16 inputs
 // span fp32's range (a training step's dO is often 1e-5 .. 1e-8, and q, k, v may exceed
@@ -104,25 +106,6 @@ __device__ __forceinline__ void red_add4(float* addr, float x, float y, float z,
                : "memory");
 }
 
-// 4 x 4 transpose inside each group of 4 lanes: lane b holds x[k] = M[row b][col k]; on
-// return it holds x[k] = M[row k][col b] (two butterfly rounds of shuffles).
-__device__ __forceinline__ void quad_transpose(float (&x)[4], int lane) {
-  const bool odd = lane & 1, hi = lane & 2;
-  float s0 = odd ? x[0] : x[1], s1 = odd ? x[2] : x[3];
-  float r0 = __shfl_xor_sync(0xffffffffu, s0, 1), r1 = __shfl_xor_sync(0xffffffffu, s1, 1);
-  float y0 = odd ? r0 : x[0], y1 = odd ? x[1] : r0;
-  float y2 = odd ? r1 : x[2], y3 = odd ? x[3] : r1;
-  s0 = hi ? y0 : y2;
-  s1 = hi ? y1 : y3;
-  r0 = __shfl_xor_sync(0xffffffffu, s0, 2);
-  r1 = __shfl_xor_sync(0xffffffffu, s1, 2);
-  x[0] = hi ? r0 : y0;
-  x[1] = hi ? r1 : y1;
-  x[2] = hi ? y2 : r0;
-  x[3] = hi ? y3 : r1;
-}
-
-
 // Item -> (first query row, local query head): the 64-row query tiles that see this key
 // block (from the diagonal on) and, within a tile, the group's heads.
 __device__ __forceinline__ void item_coords(int it, int nb, int gg, int group, int& q0, int& hh) {
@@ -167,10 +150,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = rem - gg * a.nkb;                         // key block; 0 (most work) first
   const int nqi = (a.S - nb * BN + BMI - 1) / BMI;         // 64-row query tiles that see it
   const int n_items = a.group * nqi;
-  // element extents for the debug checks: row terms [P][hl][S], dQ [P][S][hl][D], dK/dV
-  // [P][S][gl][D]
+  // element extents for the debug checks: row terms [P][hl][S], dQ accumulator
+  // [P][S4/4][hl][D][4], dK/dV [P][S][gl][D]
+  const int S4 = (a.S + 3) & ~3;
   const uint64_t n_ranks = gridDim.x / (uint64_t)per_rank;
-  const uint64_t ext_rows = n_ranks * a.hl * a.S, ext_q = n_ranks * a.S * a.hl * D,
+  const uint64_t ext_rows = n_ranks * a.hl * a.S, ext_q = n_ranks * S4 * a.hl * D,
                  ext_kv = n_ranks * a.S * a.gl * D;
   (void)ext_rows; (void)ext_q; (void)ext_kv;
 
@@ -477,22 +461,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       group_arrive(&dq_free[X]);
       if (has_d) {
-        // After a 4 x 4 transpose within each group of 4 lanes, lane 4g + b holds d values
-        // 32*quarter + 4g .. +3 of query row 4c + b: one 16-byte vector reduction each.
-        const int g4 = lane >> 2, b4 = lane & 3;
-        float* ptr = a.dq_acc + (((size_t)r * a.S + q0 + 32 * w2 + b4) * a.hl + hh) * D +
-                     32 * quarter + 4 * g4;
-        const int rs = a.hl * D;
-        const bool full = q0 + 32 * w2 + 32 <= a.S;
+        // The accumulator keeps four consecutive query rows of one (head, d) together
+        // ([P][S4/4][hl][D][4]), so lane d adds its rows 4c .. 4c+3 with one 16-byte
+        // reduction and a warp's 32 lanes cover 512 contiguous bytes.
+        float* ptr = a.dq_acc +
+                     ((((size_t)r * (S4 / 4) + (q0 + 32 * w2) / 4) * a.hl + hh) * D +
+                      32 * quarter + lane) * 4;
+        const size_t step = (size_t)a.hl * D * 4;   // the next four rows
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          float x[4] = {__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                        __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3])};
-          quad_transpose(x, lane);
-          if ((full || q0 + 32 * w2 + 4 * c + b4 < a.S) &&
-              ULY_IN_BOUNDS(ptr + 4 * c * rs - a.dq_acc, 4, ext_q))
-            red_add4(ptr + 4 * c * rs, x[0], x[1], x[2], x[3]);
-        }
+        for (int c = 0; c < 8; ++c)
+          if (q0 + 32 * w2 + 4 * c < a.S && ULY_IN_BOUNDS(ptr + c * step - a.dq_acc, 4, ext_q))
+            red_add4(ptr + c * step, __uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                     __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
       }
     }
     // dV (warps 0-7) and dK (8-15) of this key block, once every MMA has finished.
@@ -653,8 +633,8 @@ __global__ void __launch_bounds__(256) bwd_amax_kernel(const uint4* __restrict__
 }
 
 // D'_i = 2^(edo+ev) sum_d dO_i[d] * (O_i[d] + O_lo_i[d]) (fp32), zeroing of the dQ
-// accumulator rows and the fp16 copies q' = 2^eq q and dO' = 2^edo dO.  16 threads per row
-// of D = 128 (8 elements each), 8 per row of D = 64.
+// accumulator (acc8 groups of 8 floats, one per thread) and the fp16 copies q' = 2^eq q and
+// dO' = 2^edo dO.  16 threads per row of D = 128 (8 elements each), 8 per row of D = 64.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ o_lo,
@@ -664,7 +644,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
                                                       float* __restrict__ dq_acc,
                                                       uint4* __restrict__ q16,
                                                       uint4* __restrict__ do16, int64_t rows,
-                                                      int64_t S, int hl,
+                                                      int64_t S, int hl, int64_t acc8,
                                                       const int* __restrict__ exps) {
   constexpr int TPR = D / 8;
   const int4 ex = *reinterpret_cast<const int4*>(exps);
@@ -672,6 +652,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   const int64_t rowid = tid / TPR;       // row in [P][S][hl] order
   const int part = (int)(tid % TPR);
   float acc = 0.f;
+  if (tid < acc8 && ULY_IN_BOUNDS(tid * 8, 8, (uint64_t)acc8 * 8)) {
+    float4* zq = reinterpret_cast<float4*>(dq_acc + tid * 8);
+    zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   if (rowid < rows && ULY_IN_BOUNDS(rowid * D + part * 8, 8, (uint64_t)rows * D)) {
     const uint4 a = *reinterpret_cast<const uint4*>(o + rowid * D + part * 8);
     const uint4 b = *reinterpret_cast<const uint4*>(d_o + rowid * D + part * 8);
@@ -687,9 +672,6 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
       acc = fmaf(x.x + z.x, y.x, acc);
       acc = fmaf(x.y + z.y, y.y, acc);
     }
-    float4* zq = reinterpret_cast<float4*>(dq_acc + rowid * D + part * 8);
-    zq[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-    zq[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     // fp16 copies of dO' and q' for the main kernel's tensor-core operands
     do16[(rowid * D + part * 8) / 8] = bf16x8_to_f16x8_scaled(b, exp2i(ex.w));
     q16[(rowid * D + part * 8) / 8] = bf16x8_to_f16x8_scaled(
@@ -717,23 +699,47 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const uint4* __restrict__ s
     dst[i] = bf16x8_to_f16x8_scaled(src[i], p2);
 }
 
-// fp32 dQ accumulator (which holds 2^(kp+edo+ev+ek) dQ) -> bf16 dQ.
-__global__ void __launch_bounds__(256) bwd_dq_kernel(const float* __restrict__ acc,
-                                                     __nv_bfloat16* __restrict__ dq, int64_t n8,
+// fp32 dQ accumulator ([P][S4/4][hl][D][4] with S4 = S rounded up to a multiple of 4,
+// holding 2^(kp+edo+ev+ek) dQ) -> bf16 dQ [P][S][hl][D].  One thread per (rank, four rows,
+// head, 8 d): 128 contiguous bytes in, one 16-byte store per row out.
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const float4* __restrict__ acc,
+                                                     __nv_bfloat16* __restrict__ dq, int64_t S,
+                                                     int hl, int D, int64_t n,
                                                      const int* __restrict__ exps, int kp) {
   const int4 ex = *reinterpret_cast<const int4*>(exps);
   const int sh = -(kp + ex.w + ex.z + ex.y);
   const float m1 = exp2i(sh / 2), m2 = exp2i(sh - sh / 2);   // 2^sh, same-sign factors
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n8;
+  const int64_t S4q = (S + 3) / 4;
+  const int d8n = D / 8;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 b = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    uint4 v;
-    v.x = pack_bf16x2(a.x * m1 * m2, a.y * m1 * m2);
-    v.y = pack_bf16x2(a.z * m1 * m2, a.w * m1 * m2);
-    v.z = pack_bf16x2(b.x * m1 * m2, b.y * m1 * m2);
-    v.w = pack_bf16x2(b.z * m1 * m2, b.w * m1 * m2);
-    reinterpret_cast<uint4*>(dq)[i] = v;
+    const int d8 = (int)(i % d8n);
+    int64_t t = i / d8n;
+    const int hh = (int)(t % hl);
+    t /= hl;
+    const int64_t q4 = t % S4q, r = t / S4q;
+    const int64_t src = ((r * S4q + q4) * hl + hh) * D + 8 * d8;   // in float4 (4 rows)
+    if (!ULY_IN_BOUNDS(src, 8, (uint64_t)n * 8)) continue;
+    float4 f[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) f[j] = acc[src + j];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t qrow = 4 * q4 + k;
+      if (qrow >= S) break;
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        x[j] = (k == 0 ? f[j].x : k == 1 ? f[j].y : k == 2 ? f[j].z : f[j].w) * m1 * m2;
+      uint4 o;
+      o.x = pack_bf16x2(x[0], x[1]);
+      o.y = pack_bf16x2(x[2], x[3]);
+      o.z = pack_bf16x2(x[4], x[5]);
+      o.w = pack_bf16x2(x[6], x[7]);
+      const int64_t dst = ((r * S + qrow) * hl + hh) * D + 8 * d8;
+      if (ULY_IN_BOUNDS(dst, 8, (uint64_t)(n / S4q) * S * 8))
+        *reinterpret_cast<uint4*>(dq + dst) = o;
+    }
   }
 }
 
@@ -773,12 +779,14 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
         static_cast<const uint4*>(d_o), nq8, nk8, scal, std::ldexp(p.scale, kp), D, p.status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int64_t threads = rows * (D / 8);
+    // the accumulator covers S rounded up to a multiple of 4 rows (S4 >= S)
+    const int64_t acc8 = (int64_t)p.P * ((p.S + 3) & ~(int64_t)3) * hl * D / 8;
+    const int64_t threads = std::max<int64_t>(rows * (D / 8), acc8);
     const int64_t blocks = (threads + 255) / 256;
     bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(o_lo),
         static_cast<const __nv_bfloat16*>(d_o), static_cast<const __nv_bfloat16*>(q), delta,
-        dq_acc, static_cast<uint4*>(q16), static_cast<uint4*>(do16), rows, p.S, hl, exps);
+        dq_acc, static_cast<uint4*>(q16), static_cast<uint4*>(do16), rows, p.S, hl, acc8, exps);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t b8 = std::min<int64_t>((nk8 + 255) / 256, cap);
@@ -828,10 +836,11 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   attn_bwd_kernel<D><<<(unsigned)blocks, kThreads, BwdLayout<D>::kBytes, st>>>(tq, tk, tv, tdo, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t n8 = rows * D / 8;
-  const int64_t blocks_dq = std::min<int64_t>((n8 + 255) / 256, cap);
-  bwd_dq_kernel<<<(unsigned)blocks_dq, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dq), n8,
-                                                     exps, kp);
+  const int64_t n_dq = (int64_t)p.P * ((p.S + 3) / 4) * hl * (D / 8);
+  const int64_t blocks_dq = std::min<int64_t>((n_dq + 255) / 256, cap);
+  bwd_dq_kernel<<<(unsigned)blocks_dq, 256, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                     static_cast<__nv_bfloat16*>(dq), p.S, hl, D,
+                                                     n_dq, exps, kp);
   return cudaGetLastError();
 }
 
@@ -842,7 +851,7 @@ BwdWorkspace bwd_workspace_layout(const Plan& p) {
   auto al = [](size_t x) { return (x + 255) & ~size_t(255); };
   BwdWorkspace w;
   size_t off = 0;
-  w.dq_acc = off; off += al(P * S * hl * D * sizeof(float));
+  w.dq_acc = off; off += al(P * ((S + 3) & ~size_t(3)) * hl * D * sizeof(float));
   w.delta = off;  off += al(P * hl * S * sizeof(float));
   w.q16 = off;    off += al(P * S * hl * D * 2);
   w.do16 = off;   off += al(P * S * hl * D * 2);

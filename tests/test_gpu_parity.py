@@ -129,6 +129,7 @@ ATTN_CASES = [  # S, P, H, G, D, std of q/k/v
     (1000, 4, 8, 4, 128, 1.0),       # ragged tail, GQA 2:1
     (384, 2, 4, 2, 64, 1.0),         # odd number of 128-row tiles
     (130, 1, 2, 1, 128, 1.0),        # one rank, tail of 2 rows
+    (1002, 2, 4, 2, 64, 1.0),        # two ranks, S % 4 = 2 (the dQ accumulator pads rows)
     (8, 8, 8, 8, 64, 1.0),           # one token per rank
     (4096, 16, 32, 16, 128, 1.0),    # 16 ranks: two query heads and one KV head per rank
     (2048, 4, 32, 4, 128, 1.28),     # GQA 8:1
