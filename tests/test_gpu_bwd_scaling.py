@@ -85,9 +85,13 @@ def test_power_of_two_scaling_is_exact():
     assert torch.equal(l1, l0)
     assert np.array_equal(dv1, dv0 * 2.0 ** c)
     assert np.array_equal(dk1, dk0 * 2.0 ** (a + b + c))
-    # dQ's fp32 atomic additions run in no fixed order: at most one bf16 step apart
+    # dQ's fp32 atomic additions (one per 128-key block) run in no fixed order.  Reordering
+    # them changes the sum by the fp32 rounding of the partial sums, at most about
+    # (S / 128) * 2^-24 * max|partial| <= 2^-20 max|dQ| here; where the sum cancels that
+    # exceeds the bf16 spacing of the small result.  So: one bf16 step, or 2^-16 max|dQ|.
     d = np.abs(dq1 * 2.0 ** -(b + c - a) - dq0)
-    assert np.all(d <= bf16_ulp(dq0)) and d.mean() < 1e-4, (d.max(), d.mean())
+    bound = np.maximum(bf16_ulp(dq0), 2.0 ** -16 * np.abs(dq0).max())
+    assert np.all(d <= bound) and d.mean() < 1e-4, (d.max(), d.mean(), (d / bound).max())
     # and the scaled case against the oracle, scaled back
     qf, kf, vf, dof = (synthetic.bf16_to_f64(t) for t in (qs, ks, vs, dos))
     for r in (0, P - 1):
