@@ -60,15 +60,15 @@ def attn_flops(S, H, D):
 
 # DRAM bytes of one ulysses_attn_bwd call at the bench workload (S=131072), summed over its six
 # kernels (dram__bytes_read.sum + dram__bytes_write.sum, one pass each, --clock-control none):
-# attn_bwd_kernel from one capture of that kernel alone, one launch, at S=131072 (17.57 GB read,
-# 8.84 GB written); the five streaming kernels (largest magnitudes, pre-pass, two fp16 copies, dQ
-# conversion), whose bytes are a fixed number per element, from a capture of one call at S=32768
-# scaled by 4.  Valid only for the kernel source it was taken on: the figure is dropped (null) as
-# soon as the hash of that source changes.
-BWD_TRAFFIC = {"bytes": (17.569 + 8.838) * 1e9 + 4 * (0.673954 + 2.102759 + 0.081413 + 0.081357
-                                                    + 0.771625) * 1e9,
+# attn_bwd_kernel and bwd_dq_kernel each from a capture of that kernel alone at S=131072
+# (17.57 GB read + 8.84 GB written; 2.148 + 1.045 GB); the other four streaming kernels
+# (largest magnitudes, pre-pass, two fp16 copies), whose bytes are a fixed number per element,
+# from a capture of one call at S=32768 scaled by 4.  Valid only for the kernel source it was
+# taken on: the figure is dropped (null) as soon as the hash of that source changes.
+BWD_TRAFFIC = {"bytes": (17.569 + 8.838) * 1e9 + (2.148 + 1.045) * 1e9
+                        + 4 * (0.673954 + 2.102759 + 0.081413 + 0.081357) * 1e9,
                "seq_len": 131072,
-               "source_sha256": "583496fad9ec3543f5ec8a0811eae26a783e8f38fab0fc47a47d17eb9f82fe77"}
+               "source_sha256": "dbe1906bf75f3a355795b09b5bf401a6346b3d5a72e4498ed604357326d48348"}
 
 
 def bwd_traffic(seq_len):

@@ -700,46 +700,63 @@ __global__ void __launch_bounds__(256) to_f16_kernel(const uint4* __restrict__ s
 }
 
 // fp32 dQ accumulator ([P][S4/4][hl][D][4] with S4 = S rounded up to a multiple of 4,
-// holding 2^(kp+edo+ev+ek) dQ) -> bf16 dQ [P][S][hl][D].  One thread per (rank, four rows,
-// head, 8 d): 128 contiguous bytes in, one 16-byte store per row out.
+// holding 2^(kp+edo+ev+ek) dQ) -> bf16 dQ [P][S][hl][D].  A block reads 4 x 256 consecutive
+// float4 (each four rows of one d) into shared memory, coalesced, four independent loads per
+// thread; then each group of 8 threads, which holds 8 d of four rows, writes them as rows:
+// thread j of the group the 4 d starting at 4 (j % 2) of row j / 2 (8 bytes).  n4 (the
+// number of float4) is a multiple of 8, so a group never straddles the end.
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const float4* __restrict__ acc,
                                                      __nv_bfloat16* __restrict__ dq, int64_t S,
-                                                     int hl, int D, int64_t n,
+                                                     int hl, int D, int64_t n4,
                                                      const int* __restrict__ exps, int kp) {
+  constexpr int U = 4;
+  // per sub-tile 32 groups of 32 floats, plus one word of padding per group so that the
+  // row reads below spread over the banks
+  __shared__ float tile[U][32 * 33];
   const int4 ex = *reinterpret_cast<const int4*>(exps);
   const int sh = -(kp + ex.w + ex.z + ex.y);
   const float m1 = exp2i(sh / 2), m2 = exp2i(sh - sh / 2);   // 2^sh, same-sign factors
   const int64_t S4q = (S + 3) / 4;
-  const int d8n = D / 8;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int d8 = (int)(i % d8n);
-    int64_t t = i / d8n;
-    const int hh = (int)(t % hl);
-    t /= hl;
-    const int64_t q4 = t % S4q, r = t / S4q;
-    const int64_t src = ((r * S4q + q4) * hl + hh) * D + 8 * d8;   // in float4 (4 rows)
-    if (!ULY_IN_BOUNDS(src, 8, (uint64_t)n * 8)) continue;
-    float4 f[8];
+  const int tid = threadIdx.x, grp = tid / 8, j = tid % 8;
+  const int k = j / 2, h = j % 2;                             // output row, d half
+  for (int64_t base = (int64_t)blockIdx.x * 256 * U; base < n4;
+       base += (int64_t)gridDim.x * 256 * U) {
+    float4 v[U];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) f[j] = acc[src + j];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t qrow = 4 * q4 + k;
-      if (qrow >= S) break;
-      float x[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        x[j] = (k == 0 ? f[j].x : k == 1 ? f[j].y : k == 2 ? f[j].z : f[j].w) * m1 * m2;
-      uint4 o;
-      o.x = pack_bf16x2(x[0], x[1]);
-      o.y = pack_bf16x2(x[2], x[3]);
-      o.z = pack_bf16x2(x[4], x[5]);
-      o.w = pack_bf16x2(x[6], x[7]);
-      const int64_t dst = ((r * S + qrow) * hl + hh) * D + 8 * d8;
-      if (ULY_IN_BOUNDS(dst, 8, (uint64_t)(n / S4q) * S * 8))
-        *reinterpret_cast<uint4*>(dq + dst) = o;
+    for (int u = 0; u < U; ++u) {
+      const int64_t g = base + 256 * u + tid;
+      v[u] = (g < n4 && ULY_IN_BOUNDS(g, 1, (uint64_t)n4)) ? acc[g]
+                                                            : make_float4(0.f, 0.f, 0.f, 0.f);
     }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float* t = tile[u] + grp * 33 + j * 4;
+      t[0] = v[u].x;
+      t[1] = v[u].y;
+      t[2] = v[u].z;
+      t[3] = v[u].w;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t g0 = base + 256 * u + 8 * grp;   // the group's first float4: d = 8 d8
+      if (g0 >= n4) continue;
+      const int d = (int)(g0 % D);
+      int64_t t = g0 / D;
+      const int hh = (int)(t % hl);
+      t /= hl;
+      const int64_t q4 = t % S4q, r = t / S4q;
+      const int64_t qrow = 4 * q4 + k;
+      if (qrow >= S) continue;
+      const float* src = tile[u] + grp * 33 + (4 * h) * 4 + k;   // float4 4h + m, component k
+      uint2 o;
+      o.x = pack_bf16x2(src[0] * m1 * m2, src[4] * m1 * m2);
+      o.y = pack_bf16x2(src[8] * m1 * m2, src[12] * m1 * m2);
+      const int64_t dst = ((r * S + qrow) * hl + hh) * D + d + 4 * h;
+      if (ULY_IN_BOUNDS(dst, 4, (uint64_t)(n4 / S4q) * S))
+        *reinterpret_cast<uint2*>(dq + dst) = o;
+    }
+    __syncthreads();
   }
 }
 
@@ -836,11 +853,11 @@ cudaError_t launch_bwd_d(const Plan& p, const void* q, const void* k, const void
   attn_bwd_kernel<D><<<(unsigned)blocks, kThreads, BwdLayout<D>::kBytes, st>>>(tq, tk, tv, tdo, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const int64_t n_dq = (int64_t)p.P * ((p.S + 3) / 4) * hl * (D / 8);
-  const int64_t blocks_dq = std::min<int64_t>((n_dq + 255) / 256, cap);
+  const int64_t n4 = (int64_t)p.P * ((p.S + 3) / 4) * hl * D;   // float4 of the accumulator
+  const int64_t blocks_dq = std::min<int64_t>((n4 + 1023) / 1024, cap);
   bwd_dq_kernel<<<(unsigned)blocks_dq, 256, 0, st>>>(reinterpret_cast<const float4*>(dq_acc),
                                                      static_cast<__nv_bfloat16*>(dq), p.S, hl, D,
-                                                     n_dq, exps, kp);
+                                                     n4, exps, kp);
   return cudaGetLastError();
 }
 
